@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Throughput of Fused-Softmax MX attention on one GB300 (and N replicas).
+
+One step = the whole hot path for each of the three formats (MXFP8, MXFP6,
+MXFP4) over one batch of synthetic input: MX quantization of Q, K, V
+followed by the fused attention kernel.  `value` is the aggregate attention
+throughput 4*B*H*S^2*D per format-call over the device-timed region (inputs
+resident in HBM); `per_format` breaks it down and gives the attention
+kernel alone; `e2e` repeats the step through the public C-ABI call with the
+inputs copied in from pinned host memory and the outputs copied back.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import fsa_inputs  # noqa: E402
+
+METRIC = "fused-softmax MX attention TFLOPS per format at 1 GB300; % of MX MMA peak"
+FORMATS = ("mxfp8", "mxfp6", "mxfp4")
+WORKLOADS = {
+    # video-DiT self-attention: 21 x 45 x 80 latent tokens, 40 heads of 128
+    "video-dit": dict(B=1, H=40, S=75600, D=128),
+    "h16-s8192": dict(B=1, H=16, S=8192, D=128),
+    "rollback-stress": dict(B=1, H=8, S=32768, D=128, stress_from=16384),
+    "h32-s16384": dict(B=1, H=32, S=16384, D=128),
+    "h32-s32768": dict(B=1, H=32, S=32768, D=128),
+    "h32-s65536": dict(B=1, H=32, S=65536, D=128),
+    "h32-s131072": dict(B=1, H=32, S=131072, D=128),
+}
+THRESHOLD = 8.0
+
+
+def flops(w):
+    return 4.0 * w["B"] * w["H"] * w["S"] * w["S"] * w["D"]
+
+
+def workload_name(name, w):
+    return f"{name} B={w['B']} H={w['H']} Sq=Sk={w['S']} D={w['D']}"
+
+
+def peaks():
+    """Measured peaks; the MX rate is the measured bf16 rate times the nominal
+    fp8/bf16 ratio (4.5 / 2.25)."""
+    p = {"source": "fallback", "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        p = {"source": "measured", "bf16_burst": float(m["bf16_tflops"]),
+             "bf16_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+             "hbm_gbs": float(m["hbm_gbs"])}
+    except (OSError, KeyError, ValueError):
+        pass
+    ratio = 4.5 / 2.25
+    p["mx8_burst"] = p["bf16_burst"] * ratio
+    p["mx8_sustained"] = p["bf16_sustained"] * ratio
+    p["fp4_sustained"] = p["bf16_sustained"] * (13.5 / 2.25)
+    return p
+
+
+def traffic_from_profiles():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if one exists for the current kernel."""
+    path = os.path.join(ROOT, "profiles", "fsa_attn_fwd_kernel_video_dit.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    return float(m.group(1)) if m else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def to_dev(bits, device):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def oracle_sample(q, k, v, w, fmt, n_rows, threads):
+    """Time the oracle on n_rows query rows of the first head."""
+    import oracle
+    rows = np.linspace(0, w["S"] - 1, n_rows).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=THRESHOLD, rows=rows,
+                     threads=threads)
+    dt = time.perf_counter() - t0
+    return n_rows * 4.0 * w["S"] * w["D"], dt
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    q, k, v = fsa_inputs.qkv(w["B"], w["H"], w["S"], w["D"], seed=0,
+                             stress_from=w.get("stress_from"))
+    threads = len(os.sched_getaffinity(0))
+    n_rows = args.ref_rows
+    total_f, total_t = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        f_step, t_step = 0.0, 0.0
+        for fmt in FORMATS:
+            f, t = oracle_sample(q, k, v, w, fmt, n_rows, threads)
+            f_step += f
+            t_step += t
+        if i >= args.warmup:
+            total_f += f_step
+            total_t += t_step
+    val = total_f / total_t / 1e12
+    sample = (f"{n_rows} query rows of head 0 per format per step (all keys), "
+              f"3 formats; rate extrapolates exactly since rows are independent")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic N(0,1) bf16, seed 0",
+        "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
+                   "threshold": THRESHOLD},
+        "cpu_baseline": {"kind": "oracle", "value": val, "unit": "TFLOP/s", "cores": threads,
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fsa", choices=("fsa", "reference"))
+    ap.add_argument("--workload", default="video-dit", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=768)
+    ap.add_argument("--ref-rows", type=int, default=96)
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import matrix_core_softmax_gb300 as fsa
+    from matrix_core_softmax_gb300 import build as fsa_build
+    if rank == 0 or world == 1:
+        fsa_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+        dist.barrier()
+        fsa_build.build()
+    fsa.load()
+
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=rank, stress_from=w.get("stress_from"))
+    tq, tk, tv = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
+    o = torch.empty_like(tq)
+    ws = fsa.new_workspace(B, H, S, D, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    F = flops(w)
+
+    def step(ev=None):
+        for i, fmt in enumerate(FORMATS):
+            if ev is not None:
+                ev[i][0].record(stream)
+            fsa.attention_prepare(tq, tk, tv, ws, fmt)
+            if ev is not None:
+                ev[i][1].record(stream)
+            fsa.attention_run(ws, o, fmt, THRESHOLD)
+            if ev is not None:
+                ev[i][2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if fsa.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in FORMATS]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    st = fsa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error: {fsa.status_string(st)}")
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    if pg:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    n_calls = args.steps * len(FORMATS)
+    value = world * F * n_calls / elapsed / 1e12
+    pk = peaks()
+
+    per_format = {}
+    for i, fmt in enumerate(FORMATS):
+        t_q = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)]
+        t_a = [evs[s][i][1].elapsed_time(evs[s][i][2]) for s in range(args.steps)]
+        ka = statistics.mean(t_a) / 1e3
+        kq = statistics.mean(t_q) / 1e3
+        per_format[fmt] = {
+            "attention_kernel_ms": 1e3 * ka,
+            "quantize_ms": 1e3 * kq,
+            "attention_tflops": F / ka / 1e12,
+            "with_quantize_tflops": F / (ka + kq) / 1e12,
+            "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
+            "quantize_gbs": (3 * B * H * S * D * (2 + 1 + 1 / 32)) / kq / 1e9,
+        }
+    per_format["mxfp4"]["frac_of_fp4_qk_roofline"] = (
+        per_format["mxfp4"]["attention_tflops"] /
+        (2.0 / (1.0 / pk["fp4_sustained"] + 1.0 / pk["mx8_sustained"])))
+
+    # in-house BF16 flash-attention baseline, same inputs
+    bf16 = None
+    if not args.no_bf16:
+        fsa.bf16_attention_fwd(tq, tk, tv, out=o)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nb = max(2, args.steps)
+        e0.record(stream)
+        for _ in range(nb):
+            fsa.bf16_attention_fwd(tq, tk, tv, out=o)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tb = e0.elapsed_time(e1) / 1e3 / nb
+        bf16 = {"kernel_ms": 1e3 * tb, "tflops": F / tb / 1e12,
+                "frac_of_bf16_peak": F / tb / 1e12 / pk["bf16_sustained"]}
+        for fmt in FORMATS:
+            per_format[fmt]["speedup_vs_bf16_kernel"] = tb / (per_format[fmt]["attention_kernel_ms"] / 1e3)
+
+    # end to end through the public call: pinned host in, pinned host out
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.empty_like(t, device="cpu").pin_memory() for t in (tq, tk, tv))
+        for h, t in ((hq, tq), (hk, tk), (hv, tv)):
+            h.copy_(t)
+        ho = torch.empty_like(o, device="cpu").pin_memory()
+        dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            for fmt in FORMATS:
+                fsa.attention_fwd(dq, dk, dv, fmt=fmt, threshold=THRESHOLD, out=o)
+                ho.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = e0.elapsed_time(e1) / 1e3
+        if pg:
+            tt = torch.tensor([te], device=dev, dtype=torch.float64)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            te = float(tt.item())
+        nbytes = tq.numel() * 2
+        e2e = {"value": world * F * n_calls / te / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": len(FORMATS) * nbytes}
+        if fsa.get_device_error() != 0:
+            raise RuntimeError("device error during e2e")
+
+    if rank != 0:
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        threads = len(os.sched_getaffinity(0))
+        f, t = oracle_sample(q, k, v, w, "mxfp8", args.cpu_rows, threads)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{args.cpu_rows} query rows of head 0 (all {S} keys), MXFP8, "
+                         f"{t:.1f} s; rows are independent so the rate extrapolates exactly"}
+
+    a8 = per_format["mxfp8"]
+    roof = {"bound": "tensor", "kernel": "fsa_attn_fwd_kernel (MXFP8)",
+            "achieved": a8["attention_tflops"], "peak": pk["mx8_sustained"], "unit": "TFLOP/s",
+            "frac": a8["attention_tflops"] / pk["mx8_sustained"],
+            "peak_note": (f"{pk['source']} bf16 sustained {pk['bf16_sustained']:.1f} TFLOP/s x 2 "
+                          "(nominal fp8/bf16 ratio); burst-based peak "
+                          f"{pk['mx8_burst']:.1f}"),
+            "algorithmic_flops_per_launch": F,
+            "traffic": traffic_from_profiles()}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mx (e4m3|e2m3|e2m1 x e8m0) mma, fp32 accumulate",
+        "data": "synthetic N(0,1) bf16, seed = rank",
+        "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
+                   "threshold": THRESHOLD, "non_causal": True,
+                   "l2": f"inputs {2 * B * H * S * D / 1e6:.0f} MB each, larger than the 129 MB L2",
+                   "step": "per format: quantize Q,K,V + fused attention"},
+        "per_format": per_format,
+        "bf16_baseline": bf16,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(FORMATS) * 4,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

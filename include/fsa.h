@@ -1,0 +1,197 @@
+/*
+ * fsa.h -- C ABI of the GB300 (sm_103a) Fused-Softmax quantized attention
+ * library, libfsa.so.
+ *
+ * What the library computes is the forward pass described in
+ *   "Fused-Softmax shifts an AI attention bottleneck onto faster GPU
+ *    hardware" (article on arXiv:2611.09225), paragraphs 5-8, and
+ *   "Fused softmax makes quantized attention faster on AMD GPUs", section
+ *    "What the evidence shows", bullet "Move work, keep correction":
+ *   Q, K, V are microscaled (32-element blocks sharing one E8M0 power-of-two
+ *   scale) to MXFP8, MXFP6 or MXFP4; S = Q K^T runs on block-scaled tensor
+ *   cores with the frozen row-max subtraction and the Schraudolph
+ *   exponential's affine map applied to the accumulator; the rounded result
+ *   is reinterpreted as a BF16 weight, converted a second time into an MX
+ *   operand P, and O = P V and l = P 1 both come from tensor-core products on
+ *   that same P.  A gate rolls the reference maximum forward when a tile's
+ *   scores pass it by more than a threshold and rescales O and l.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned.  Attention tensors are bf16, contiguous [B][H][S][D] ("BHSD").
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it; a call returns after
+ *    launching.  Argument errors are detected on the host and returned before
+ *    anything is launched.
+ *  - Device-side failures that the kernels detect themselves (a bounded wait
+ *    that ran out) are recorded in a per-device error word; read and clear it
+ *    with fsa_get_device_error().
+ *  - Only sm_103a (GB300) and sm_100a devices are supported; others get
+ *    FSA_ERR_UNSUPPORTED.
+ *  - Inputs must be finite; the output is undefined for Inf or NaN inputs.
+ */
+#ifndef FSA_H_
+#define FSA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FSA_API __attribute__((visibility("default")))
+#else
+#define FSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Attention formats ("Fused-Softmax shifts ...", paragraph 8): element type
+ * of Q/K/V and of P.  MXFP8: E4M3 / E4M3.  MXFP6: E2M3 / E2M3.
+ * MXFP4: E2M1 / E2M3 (the MXFP4 variant keeps six-bit P). */
+typedef enum { FSA_MXFP8 = 0, FSA_MXFP6 = 1, FSA_MXFP4 = 2 } fsa_format;
+
+/* Element types of fsa_quantize_mx. */
+typedef enum { FSA_ELEM_E4M3 = 0, FSA_ELEM_E2M3 = 1, FSA_ELEM_E2M1 = 2 } fsa_elem;
+
+typedef enum {
+    FSA_OK = 0,
+    FSA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, bad enum, theta */
+    FSA_ERR_UNSUPPORTED = 2,      /* device architecture or head dim D */
+    FSA_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
+    FSA_ERR_OUT_OF_MEMORY = 4,    /* workspace allocation failed */
+    FSA_ERR_TIMEOUT = 5           /* a kernel's bounded wait ran out */
+} fsa_status;
+
+/* Debug switches of fsa_options.debug_flags (test use only). */
+#define FSA_DEBUG_SKIP_KV_ARRIVE 0x1 /* the loader never signals KV tile 1:
+                                        the consumers' bounded waits run out,
+                                        the kernel exits cleanly and the error
+                                        word reads FSA_ERR_TIMEOUT */
+
+typedef struct {
+    /* Score scale; <= 0 selects 1/sqrt(D). */
+    float sm_scale;
+    /* Optional device output, [B*H*S][n_t] bytes with n_t = ceil(S/128):
+     * byte (row, t) is set to 1 when the rollback gate fired for that row at
+     * KV tile t (tile 0 initialises the reference and never fires) and to 0
+     * otherwise.  NULL: not written. */
+    uint8_t *rollback_bits;
+    /* Optional device counter; the number of gate firings is ADDED to it.
+     * NULL: not written. */
+    unsigned long long *rollback_count;
+    /* Optional caller-owned device workspace of at least
+     * fsa_attention_workspace_size() bytes, 256-byte aligned.  NULL: the
+     * library uses its own cached per-device workspace (allocated on first
+     * use and grown as needed; concurrent calls on different streams must
+     * then not overlap). */
+    void *workspace;
+    uint64_t workspace_bytes;
+    /* Bounded-wait limit of the kernels in milliseconds; <= 0 means 2000. */
+    int wait_timeout_ms;
+    int debug_flags;
+} fsa_options;
+
+/*
+ * fsa_quantize_mx -- MX microscaling of a bf16 tensor x[batch][rows][cols].
+ *
+ * Source: "EFQ-Softmax: Exp-Free Quantization for Softmax", section
+ * "B. Block-Scaled E2M1 Probability Representation" (blocks sharing an
+ * exponent-only E8M0 scale) and "Fused-Softmax shifts ...", paragraphs 7-8
+ * (MXFP8/MXFP6/MXFP4 operands).  Scale rule (the pages print none; this is
+ * the library's reading): for a block with largest magnitude amax the scale
+ * is 2^X with X the smallest integer such that amax <= max_elem * 2^X,
+ * clamped to [-127, 127]; an all-zero block has X = -127.  Elements are
+ * x / 2^X rounded to nearest, ties to even (never saturating by
+ * construction).
+ *
+ *  block_axis = 1: blocks of 32 run along cols (Q and K: along D).
+ *      codes [batch][rows][cols], scales [batch][rows][ceil(cols/32)].
+ *  block_axis = 0: blocks of 32 run along rows and the output is transposed
+ *      (V: along the keys).  codes [batch][cols][rows],
+ *      scales [batch][cols][ceil(rows/32)].
+ *  The last block of a line may be shorter than 32.
+ *  codes: one element code per byte in the low bits (E4M3: 8 bits, E2M3:
+ *         6 bits, E2M1: 4 bits), sign in the code's top bit.
+ *  scales: E8M0 bytes, X + 127.
+ *  All three pointers are device pointers; x must be 16-byte aligned when
+ *  block_axis = 1 and cols % 8 == 0 (otherwise 2-byte aligned suffices).
+ * Returns FSA_ERR_INVALID_ARGUMENT for null pointers, negative sizes, a bad
+ * elem_fmt or block_axis; FSA_OK for an empty tensor (nothing launched).
+ */
+FSA_API fsa_status fsa_quantize_mx(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                           int block_axis, int elem_fmt, uint8_t *codes, uint8_t *scales,
+                           void *stream);
+
+/*
+ * fsa_attention_fwd -- Fused-Softmax MX attention forward, non-causal,
+ * Sq = Sk = S.  q, k, v, o: bf16 device tensors [B][H][S][D].
+ *
+ * Per query row i and KV tile t of 128 keys ("Fused-Softmax shifts ...",
+ * paragraphs 5 and 6):
+ *   s_ij = sm * q^_i . k^_j (block-scaled MMA, FP32 accumulate);
+ *   tile 0 freezes m_i = max_j s_ij;  a later tile whose max passes m_i by
+ *   more than `threshold` rolls back: O_i, l_i *= exp(m_i - m'), m_i = m';
+ *   y_ij = 128 * ((s_ij - m_i) * log2(e) + 127) - 7;  code = clamp(rne(y), 0,
+ *   0x7F7F) read as a bf16 p_ij;  P^ = MX(p) in 32-key blocks (E4M3 for
+ *   MXFP8, E2M3 otherwise);  O_i += P^ V^, l_i += P^ 1 (both MMAs);
+ *   o_i = bf16(O_i / l_i).  Keys >= S are masked before the gate.
+ * Requirements: B, H, S >= 1; D in {64, 128}; threshold finite in [0, 80]
+ * (128 * (threshold * log2(e) + 127) must stay a finite bf16 code).
+ * Uses the library's cached workspace (see fsa_options.workspace).
+ */
+FSA_API fsa_status fsa_attention_fwd(const void *q, const void *k, const void *v, void *o,
+                             int B, int H, int S, int D, int fmt, float threshold,
+                             void *stream);
+
+/* As fsa_attention_fwd with options (NULL = defaults). */
+FSA_API fsa_status fsa_attention_fwd_ex(const void *q, const void *k, const void *v, void *o,
+                                int B, int H, int S, int D, int fmt, float threshold,
+                                const fsa_options *opt, void *stream);
+
+/*
+ * The two halves of fsa_attention_fwd_ex, for callers that keep the MX
+ * copies (e.g. quantize K/V once and attend many times) or time the parts.
+ *
+ * fsa_attention_prepare: MX-quantizes q, k, v (bf16 [B][H][S][D]) into the
+ * caller's device workspace (>= fsa_attention_workspace_size() bytes,
+ * 256-byte aligned): Q and K in 32-element blocks along D, V in 32-key
+ * blocks along the keys, stored transposed; element type per `fmt`.
+ * fsa_attention_run: the fused attention kernel on a prepared workspace;
+ * shape and fmt must be those given to fsa_attention_prepare; opt may be
+ * NULL; opt->workspace is ignored.
+ */
+FSA_API fsa_status fsa_attention_prepare(const void *q, const void *k, const void *v, int B, int H,
+                                         int S, int D, int fmt, void *workspace,
+                                         uint64_t workspace_bytes, void *stream);
+FSA_API fsa_status fsa_attention_run(const void *workspace, uint64_t workspace_bytes, void *o,
+                                     int B, int H, int S, int D, int fmt, float threshold,
+                                     const fsa_options *opt, void *stream);
+
+/* Bytes of device workspace fsa_attention_fwd needs for this shape (MX
+ * copies of Q, K, V and their scales).  0 for invalid arguments. */
+FSA_API uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fmt);
+
+/*
+ * fsa_bf16_attention_fwd -- conventional BF16 flash attention (exact
+ * softmax with a running maximum, FP32 accumulation, BF16 P), the speed
+ * and error denominator the pages compare against ("Fused-Softmax shifts
+ * ...", paragraphs 7-8).  Same tensor conventions; D in {64, 128}.
+ */
+FSA_API fsa_status fsa_bf16_attention_fwd(const void *q, const void *k, const void *v, void *o,
+                                  int B, int H, int S, int D, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: FSA_OK, FSA_ERR_TIMEOUT, or FSA_ERR_CUDA if the sync
+ * itself failed. */
+FSA_API fsa_status fsa_get_device_error(void *stream);
+
+/* Static description of a status code. */
+FSA_API const char *fsa_status_string(fsa_status s);
+
+/* Frees the library's cached workspaces on every device (synchronising). */
+FSA_API void fsa_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FSA_H_ */

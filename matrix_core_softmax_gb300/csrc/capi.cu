@@ -1,0 +1,413 @@
+// capi.cu -- the C ABI of libfsa.so (declared in include/fsa.h): argument
+// validation, the cached per-device workspace, TMA tensor maps and launches.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "fsa.h"
+#include "fsa_internal.h"
+
+namespace fsa {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    std::mutex mu;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    unsigned int* err = nullptr;
+    int arch_ok = -1;  // -1 unknown, 0 no, 1 yes
+};
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D byte tensor map: dims (inner first), row strides in bytes, box.
+bool make_map_u8(CUtensorMap* m, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1,
+                 CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1, stride2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map.
+bool make_map_bf16(CUtensorMap* m, void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1,
+                   CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {stride1, stride2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Current device, its state, and the architecture check (sm_100 / sm_103).
+fsa_status current_device(int* dev_out, DeviceState** st_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FSA_ERR_UNSUPPORTED;
+    DeviceState& st = g_dev[dev];
+    std::lock_guard<std::mutex> lk(st.mu);
+    if (st.arch_ok < 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        st.arch_ok = (major == 10 && (minor == 0 || minor == 3)) ? 1 : 0;
+    }
+    if (!st.arch_ok) return FSA_ERR_UNSUPPORTED;
+    if (!st.err) {
+        if (cudaMalloc(&st.err, sizeof(unsigned int)) != cudaSuccess) return FSA_ERR_OUT_OF_MEMORY;
+        if (cudaMemset(st.err, 0, sizeof(unsigned int)) != cudaSuccess) return FSA_ERR_CUDA;
+    }
+    *dev_out = dev;
+    *st_out = &st;
+    return FSA_OK;
+}
+
+fsa_status validate_attention(const void* q, const void* k, const void* v, const void* o, int B,
+                              int H, int S, int D) {
+    if (!q || !k || !v || !o) return FSA_ERR_INVALID_ARGUMENT;
+    if (B < 1 || H < 1 || S < 1) return FSA_ERR_INVALID_ARGUMENT;
+    if (D != 64 && D != 128) return FSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * H > 65535) return FSA_ERR_INVALID_ARGUMENT;
+    if (S > (1 << 30)) return FSA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return FSA_ERR_INVALID_ARGUMENT;
+    return FSA_OK;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int64_t BH, int64_t S, int D) {
+    const int64_t S16 = (S + 15) / 16 * 16;
+    const int64_t nt = (S + kTile - 1) / kTile;
+    return align256(BH * S * D) * 2 + align256(BH * D * S16) +
+           align256(3 * BH * nt * static_cast<int64_t>(kAtomBytes));
+}
+
+AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t S, int D) {
+    const int64_t S16 = (S + 15) / 16 * 16;
+    const int64_t nt = (S + kTile - 1) / kTile;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    AttnWorkspace w{};
+    w.qc = p; p += align256(BH * S * D);
+    w.kc = p; p += align256(BH * S * D);
+    w.vt = p; p += align256(BH * D * S16);
+    const size_t atoms = static_cast<size_t>(BH * nt) * kAtomBytes;
+    w.qsf = p;
+    w.ksf = p + atoms;
+    w.vsf = p + 2 * atoms;
+    w.sf_bytes_total = 3 * atoms;
+    return w;
+}
+
+}  // namespace fsa
+
+namespace fsa {
+namespace {
+
+fsa_status check_run_args(int fmt, float threshold, const fsa_options& op) {
+    if (fmt < 0 || fmt > 2) return FSA_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(threshold) || threshold < 0.0f || threshold > 80.0f)
+        return FSA_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(op.sm_scale)) return FSA_ERR_INVALID_ARGUMENT;
+    return FSA_OK;
+}
+
+fsa_status check_workspace(const void* ws, uint64_t bytes, int64_t BH, int S, int D) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return FSA_ERR_INVALID_ARGUMENT;
+    if (bytes < attn_workspace_bytes(BH, S, D)) return FSA_ERR_INVALID_ARGUMENT;
+    return FSA_OK;
+}
+
+// Quantizes Q, K (blocks along D) and V (blocks along keys, transposed).
+fsa_status prepare_impl(const void* q, const void* k, const void* v, int64_t BH, int S, int D,
+                        int fmt, void* ws_base, cudaStream_t st) {
+    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, S, D);
+    const int elem = fmt == FSA_MXFP8 ? ELEM_E4M3 : (fmt == FSA_MXFP6 ? ELEM_E2M3 : ELEM_E2M1);
+    const int64_t S16 = (static_cast<int64_t>(S) + 15) / 16 * 16;
+    if (cudaMemsetAsync(ws.qsf, 0x7F, ws.sf_bytes_total, st) != cudaSuccess) return FSA_ERR_CUDA;
+    if (launch_quant_rows(static_cast<const uint16_t*>(q), BH * S, D, elem, QL_ATTN, ws.qc, ws.qsf,
+                          S, st) != cudaSuccess ||
+        launch_quant_rows(static_cast<const uint16_t*>(k), BH * S, D, elem, QL_ATTN, ws.kc, ws.ksf,
+                          S, st) != cudaSuccess ||
+        launch_quant_cols(static_cast<const uint16_t*>(v), BH, S, D, elem, QL_ATTN, ws.vt, S16,
+                          ws.vsf, st) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    return FSA_OK;
+}
+
+// The fused attention kernel on a prepared workspace.
+fsa_status run_impl(void* ws_base, void* o, int64_t BH, int S, int D, int fmt, float threshold,
+                    const fsa_options& op, unsigned int* err, cudaStream_t st) {
+    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, S, D);
+    const int64_t S16 = (static_cast<int64_t>(S) + 15) / 16 * 16;
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapSwizzle qk_swz =
+        D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map_u8(&tq, ws.qc, D, S, BH, D, static_cast<uint64_t>(S) * D, D, kTile, qk_swz) ||
+        !make_map_u8(&tk, ws.kc, D, S, BH, D, static_cast<uint64_t>(S) * D, D, kTile, qk_swz) ||
+        !make_map_u8(&tv, ws.vt, S16, D, BH, S16, static_cast<uint64_t>(S16) * D, kTile, D,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return FSA_ERR_CUDA;
+    AttnLaunch a{};
+    a.tm_q = &tq;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    a.ws = ws;
+    a.o = o;
+    a.BH = BH;
+    a.S = S;
+    a.D = D;
+    a.fmt = fmt;
+    a.sm_scale = op.sm_scale > 0.0f ? op.sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+    a.threshold = threshold;
+    a.rollback_bits = op.rollback_bits;
+    a.rollback_count = op.rollback_count;
+    a.timeout_ns = static_cast<uint64_t>(op.wait_timeout_ms > 0 ? op.wait_timeout_ms : 2000) *
+                   1000000ull;
+    a.debug_flags = op.debug_flags;
+    a.err_word = err;
+    return launch_fsa_attention(a, st) == cudaSuccess ? FSA_OK : FSA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fsa
+
+using namespace fsa;
+
+extern "C" {
+
+const char* fsa_status_string(fsa_status s) {
+    switch (s) {
+        case FSA_OK: return "ok";
+        case FSA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case FSA_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case FSA_ERR_CUDA: return "CUDA error";
+        case FSA_ERR_OUT_OF_MEMORY: return "out of device memory";
+        case FSA_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+fsa_status fsa_quantize_mx(const void* x, int64_t batch, int64_t rows, int64_t cols,
+                           int block_axis, int elem_fmt, uint8_t* codes, uint8_t* scales,
+                           void* stream) {
+    if (!x || !codes || !scales) return FSA_ERR_INVALID_ARGUMENT;
+    if (batch < 0 || rows < 0 || cols < 0) return FSA_ERR_INVALID_ARGUMENT;
+    if (elem_fmt < 0 || elem_fmt > 2 || (block_axis != 0 && block_axis != 1))
+        return FSA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(x) & 1) != 0) return FSA_ERR_INVALID_ARGUMENT;
+    if (block_axis == 0 && (batch > 65535 || cols > (int64_t(65535) * 128)))
+        return FSA_ERR_INVALID_ARGUMENT;
+    if (batch == 0 || rows == 0 || cols == 0) return FSA_OK;
+    int dev;
+    DeviceState* ds;
+    fsa_status s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (block_axis == 1)
+        e = launch_quant_rows(static_cast<const uint16_t*>(x), batch * rows, cols, elem_fmt,
+                              QL_PLAIN, codes, scales, 0, st);
+    else
+        e = launch_quant_cols(static_cast<const uint16_t*>(x), batch, rows, cols, elem_fmt,
+                              QL_PLAIN, codes, rows, scales, st);
+    return e == cudaSuccess ? FSA_OK : FSA_ERR_CUDA;
+}
+
+uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fmt) {
+    if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128) || fmt < 0 || fmt > 2) return 0;
+    return attn_workspace_bytes(static_cast<int64_t>(B) * H, S, D);
+}
+
+fsa_status fsa_attention_prepare(const void* q, const void* k, const void* v, int B, int H, int S,
+                                 int D, int fmt, void* workspace, uint64_t workspace_bytes,
+                                 void* stream) {
+    fsa_status s = validate_attention(q, k, v, q, B, H, S, D);
+    if (s != FSA_OK) return s;
+    if (fmt < 0 || fmt > 2) return FSA_ERR_INVALID_ARGUMENT;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    s = check_workspace(workspace, workspace_bytes, BH, S, D);
+    if (s != FSA_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    return prepare_impl(q, k, v, BH, S, D, fmt, workspace, static_cast<cudaStream_t>(stream));
+}
+
+fsa_status fsa_attention_run(const void* workspace, uint64_t workspace_bytes, void* o, int B,
+                             int H, int S, int D, int fmt, float threshold, const fsa_options* opt,
+                             void* stream) {
+    fsa_status s = validate_attention(o, o, o, o, B, H, S, D);
+    if (s != FSA_OK) return s;
+    fsa_options defaults{};
+    const fsa_options& op = opt ? *opt : defaults;
+    s = check_run_args(fmt, threshold, op);
+    if (s != FSA_OK) return s;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    s = check_workspace(workspace, workspace_bytes, BH, S, D);
+    if (s != FSA_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    return run_impl(const_cast<void*>(workspace), o, BH, S, D, fmt, threshold, op, ds->err,
+                    static_cast<cudaStream_t>(stream));
+}
+
+fsa_status fsa_attention_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
+                                int H, int S, int D, int fmt, float threshold,
+                                const fsa_options* opt, void* stream) {
+    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    if (s != FSA_OK) return s;
+    fsa_options defaults{};
+    const fsa_options& op = opt ? *opt : defaults;
+    s = check_run_args(fmt, threshold, op);
+    if (s != FSA_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const size_t need = attn_workspace_bytes(BH, S, D);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (op.workspace) {
+        s = check_workspace(op.workspace, op.workspace_bytes, BH, S, D);
+        if (s != FSA_OK) return s;
+        s = prepare_impl(q, k, v, BH, S, D, fmt, op.workspace, st);
+        if (s != FSA_OK) return s;
+        return run_impl(op.workspace, o, BH, S, D, fmt, threshold, op, ds->err, st);
+    }
+    // library-owned cached workspace, grown on demand; the lock serialises
+    // host-side use of it
+    std::lock_guard<std::mutex> lk(ds->mu);
+    if (ds->ws_bytes < need) {
+        if (ds->ws) {
+            cudaDeviceSynchronize();
+            cudaFree(ds->ws);
+            ds->ws = nullptr;
+            ds->ws_bytes = 0;
+        }
+        if (cudaMalloc(&ds->ws, need) != cudaSuccess) {
+            cudaGetLastError();
+            return FSA_ERR_OUT_OF_MEMORY;
+        }
+        ds->ws_bytes = need;
+    }
+    s = prepare_impl(q, k, v, BH, S, D, fmt, ds->ws, st);
+    if (s != FSA_OK) return s;
+    return run_impl(ds->ws, o, BH, S, D, fmt, threshold, op, ds->err, st);
+}
+
+fsa_status fsa_attention_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
+                             int S, int D, int fmt, float threshold, void* stream) {
+    return fsa_attention_fwd_ex(q, k, v, o, B, H, S, D, fmt, threshold, nullptr, stream);
+}
+
+fsa_status fsa_bf16_attention_fwd(const void* q, const void* k, const void* v, void* o, int B,
+                                  int H, int S, int D, void* stream) {
+    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    if (s != FSA_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    CUtensorMap tq, tk, tv;
+    // bf16 rows of D elements: 128 (D = 64) or 256 (D = 128) bytes, loaded
+    // as boxes of 64 elements (128 bytes, one 128-byte swizzle span)
+    if (!make_map_bf16(&tq, const_cast<void*>(q), D, S, BH, 2ull * D, 2ull * S * D, 64, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tk, const_cast<void*>(k), D, S, BH, 2ull * D, 2ull * S * D, 64, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tv, const_cast<void*>(v), D, S, BH, 2ull * D, 2ull * S * D, 64, kTile,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return FSA_ERR_CUDA;
+    Bf16Launch a{};
+    a.tm_q = &tq;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    a.o = o;
+    a.BH = BH;
+    a.S = S;
+    a.D = D;
+    a.sm_scale = 1.0f / std::sqrt(static_cast<float>(D));
+    a.timeout_ns = 2000ull * 1000000ull;
+    a.err_word = ds->err;
+    return launch_bf16_attention(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FSA_OK
+               : FSA_ERR_CUDA;
+}
+
+fsa_status fsa_get_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FSA_ERR_CUDA;
+    int dev;
+    DeviceState* ds;
+    fsa_status s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    unsigned int w = 0;
+    if (cudaMemcpy(&w, ds->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FSA_ERR_CUDA;
+    if (w) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FSA_ERR_CUDA;
+    }
+    return (w & kErrTimeout) ? FSA_ERR_TIMEOUT : FSA_OK;
+}
+
+void fsa_release_workspace(void) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (int d = 0; d < n && d < kMaxDevices; ++d) {
+        std::lock_guard<std::mutex> lk(g_dev[d].mu);
+        if (g_dev[d].ws) {
+            cudaSetDevice(d);
+            cudaDeviceSynchronize();
+            cudaFree(g_dev[d].ws);
+            g_dev[d].ws = nullptr;
+            g_dev[d].ws_bytes = 0;
+        }
+    }
+    cudaSetDevice(cur);
+}
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+// quantize.cu -- MX microscaling of bf16 tensors (32-element blocks, one
+// shared E8M0 scale each) for MXFP8 (E4M3), MXFP6 (E2M3) and MXFP4 (E2M1).
+//
+// Method: "Fused-Softmax shifts an AI attention bottleneck onto faster GPU
+// hardware", paragraphs 7-8 (MX operands of the three formats) and
+// "EFQ-Softmax: Exp-Free Quantization for Softmax", section "B. Block-Scaled
+// E2M1 Probability Representation" (exponent-only block scale).  The scale
+// rule -- the smallest power of two 2^X with amax <= max_elem * 2^X -- is
+// this library's reading; the pages print none.
+//
+// Both kernels stream their input once and write codes + scales once: they
+// are HBM-bound, so the design goal is full-sector, coalesced traffic.
+#include <cuda_bf16.h>
+
+#include "fsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace fsa {
+namespace {
+
+struct FmtConsts {
+    int emax;       // exponent of the largest finite element
+    uint32_t mthr;  // largest element = (1 + mthr / 128) * 2^emax in bf16 mantissa units
+};
+
+__device__ __forceinline__ FmtConsts fmt_consts(int elem) {
+    if (elem == ELEM_E4M3) return {8, 0x60};  // 448 = 1.75 * 2^8
+    if (elem == ELEM_E2M3) return {2, 0x70};  // 7.5 = 1.875 * 2^2
+    return {2, 0x40};                         // 6   = 1.5 * 2^2
+}
+
+// Smallest integer X with amax <= max_elem * 2^X, clamped to [-127, 127];
+// -127 for an all-zero block.  amax is given as the bit pattern of a
+// non-negative bf16 (its magnitude bits, 15 bits).
+__device__ __forceinline__ int mx_scale_exp(uint32_t amax_bf16, FmtConsts f) {
+    if (amax_bf16 == 0) return -127;
+    int E = static_cast<int>(amax_bf16 >> 7);
+    uint32_t m = amax_bf16 & 0x7Fu;
+    int e;
+    if (E == 0) {  // bf16 subnormal: m * 2^-133, renormalise
+        int nb = 32 - __clz(m);
+        e = nb - 134;
+        m = (m << (8 - nb)) & 0x7Fu;
+    } else {
+        e = E - 127;
+    }
+    int X = e - f.emax + (m > f.mthr ? 1 : 0);
+    return min(127, max(-127, X));
+}
+
+// 2^-X as an FP32 (X in [-127, 126] for any bf16 block maximum).
+__device__ __forceinline__ float pow2_neg(int X) {
+    return __int_as_float((127 - X) << 23);
+}
+
+// Codes of two scaled values: byte 0 = code(lo), byte 1 = code(hi).
+__device__ __forceinline__ uint32_t encode_pair(int elem, float lo, float hi) {
+    if (elem == ELEM_E4M3) return cvt_e4m3x2(lo, hi);
+    if (elem == ELEM_E2M3) return cvt_e2m3x2(lo, hi);
+    uint32_t n = cvt_e2m1x2(lo, hi);
+    return (n & 0xFu) | ((n >> 4) << 8);
+}
+
+// Value of a narrow code (E2M3 or E2M1), exactly.
+__device__ __forceinline__ float decode_narrow(int elem, uint32_t c) {
+    uint32_t s, e, m;
+    float mag;
+    if (elem == ELEM_E2M3) {
+        s = (c >> 5) & 1u; e = (c >> 3) & 3u; m = c & 7u;
+        mag = e ? static_cast<float>(8u + m) * __int_as_float((127 + static_cast<int>(e) - 4) << 23)
+                : static_cast<float>(m) * 0.125f;
+    } else {
+        s = (c >> 3) & 1u; e = (c >> 1) & 3u; m = c & 1u;
+        mag = e ? static_cast<float>(2u + m) * __int_as_float((127 + static_cast<int>(e) - 2) << 23)
+                : static_cast<float>(m) * 0.5f;
+    }
+    return s ? -mag : mag;
+}
+
+// Pair of element codes -> pair of E4M3 bit patterns of the same values.
+__device__ __forceinline__ uint32_t to_e4m3_container(int elem, uint32_t pair) {
+    if (elem == ELEM_E4M3) return pair;
+    return cvt_e4m3x2(decode_narrow(elem, pair & 0xFFu), decode_narrow(elem, (pair >> 8) & 0xFFu));
+}
+
+// Quantizes 32 values v[] (n valid, rest zero) held as bf16 bit patterns.
+// Writes 8 words of packed codes (4 per word, element i in byte i % 4 of
+// word i / 4) and returns X.
+__device__ __forceinline__ int quantize_block32(const uint32_t (&h)[32], int elem, int layout,
+                                                uint32_t (&w)[8]) {
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = max(amax, h[i] & 0x7FFFu);
+    const int X = mx_scale_exp(amax, fmt_consts(elem));
+    const float sc = pow2_neg(X);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float a = __uint_as_float(h[4 * i + 0] << 16) * sc;
+        float b = __uint_as_float(h[4 * i + 1] << 16) * sc;
+        float c = __uint_as_float(h[4 * i + 2] << 16) * sc;
+        float d = __uint_as_float(h[4 * i + 3] << 16) * sc;
+        uint32_t p0 = encode_pair(elem, a, b), p1 = encode_pair(elem, c, d);
+        if (layout == QL_ATTN) {
+            p0 = to_e4m3_container(elem, p0);
+            p1 = to_e4m3_container(elem, p1);
+        }
+        w[i] = (p0 & 0xFFFFu) | (p1 << 16);
+    }
+    return X;
+}
+
+__device__ __forceinline__ int atom_offset(int64_t r_in_tile, int kb) {
+    return static_cast<int>((r_in_tile & 31) * 16 + (r_in_tile >> 5) * 4 + kb);
+}
+
+// Blocks of 32 along the last axis.  One thread per block.
+__global__ void quant_rows_kernel(const uint16_t* __restrict__ x, int64_t lines, int64_t cols,
+                                  int elem, int layout, uint8_t* __restrict__ codes,
+                                  uint8_t* __restrict__ scales, int64_t rows_per_mat, int vec) {
+    const int64_t nblk = (cols + 31) / 32;
+    const int64_t total = lines * nblk;
+    const int64_t n_tiles = (rows_per_mat + kTile - 1) / kTile;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t line = idx / nblk;
+        const int kb = static_cast<int>(idx - line * nblk);
+        const int64_t c0 = static_cast<int64_t>(kb) * 32;
+        const int n = static_cast<int>(cols - c0 < 32 ? cols - c0 : 32);
+        const uint16_t* src = x + line * cols + c0;
+        uint32_t h[32];
+        if (vec && n == 32) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 u = __ldg(s4 + i);
+                h[8 * i + 0] = u.x & 0xFFFFu; h[8 * i + 1] = u.x >> 16;
+                h[8 * i + 2] = u.y & 0xFFFFu; h[8 * i + 3] = u.y >> 16;
+                h[8 * i + 4] = u.z & 0xFFFFu; h[8 * i + 5] = u.z >> 16;
+                h[8 * i + 6] = u.w & 0xFFFFu; h[8 * i + 7] = u.w >> 16;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = i < n ? static_cast<uint32_t>(__ldg(src + i)) : 0u;
+        }
+        uint32_t w[8];
+        const int X = quantize_block32(h, elem, layout, w);
+        uint8_t* dst = codes + line * cols + c0;
+        if (vec && n == 32 && (cols % 16) == 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+            for (int i = 0; i < n; ++i) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+        }
+        const uint8_t sb = static_cast<uint8_t>(X + 127);
+        if (layout == QL_PLAIN) {
+            scales[line * nblk + kb] = sb;
+        } else {
+            const int64_t mat = line / rows_per_mat, r = line - mat * rows_per_mat;
+            scales[(mat * n_tiles + r / kTile) * kAtomBytes + atom_offset(r % kTile, kb)] = sb;
+        }
+    }
+}
+
+// Blocks of 32 along the middle axis (rows); output transposed so that each
+// block becomes 32 contiguous code bytes of line `col`.  A CTA stages a
+// 32-row x 128-column tile in shared memory with coalesced loads.
+constexpr int kColTileC = 128;
+__global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t* __restrict__ x,
+                                                         int64_t rows, int64_t cols, int elem,
+                                                         int layout, uint8_t* __restrict__ codes,
+                                                         int64_t pitch,
+                                                         uint8_t* __restrict__ scales) {
+    __shared__ uint16_t tile[32][kColTileC + 2];
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kColTileC;
+    const uint16_t* xb = x + b * rows * cols;
+    for (int i = threadIdx.x; i < 32 * kColTileC; i += blockDim.x) {
+        const int rr = i / kColTileC, cc = i % kColTileC;
+        const int64_t r = r0 + rr, c = c0 + cc;
+        tile[rr][cc] = (r < rows && c < cols) ? __ldg(xb + r * cols + c) : static_cast<uint16_t>(0);
+    }
+    __syncthreads();
+    const int cc = threadIdx.x;
+    const int64_t c = c0 + cc;
+    if (cc >= kColTileC || c >= cols) return;
+    uint32_t h[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) h[i] = tile[i][cc];
+    uint32_t w[8];
+    const int X = quantize_block32(h, elem, layout, w);
+    const int64_t nblk = (rows + 31) / 32;
+    const int kb = static_cast<int>(r0 / 32);
+    const uint8_t sb = static_cast<uint8_t>(X + 127);
+    uint8_t* dst = codes + (b * cols + c) * pitch + r0;
+    if (layout == QL_PLAIN) {
+        const int n = static_cast<int>(rows - r0 < 32 ? rows - r0 : 32);
+        for (int i = 0; i < n; ++i) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+        scales[(b * cols + c) * nblk + kb] = sb;
+    } else {
+        // pitch is a multiple of 16 and r0 of 32: each 16-byte half of the
+        // block is entirely inside or entirely outside the padded line; the
+        // padding keys [rows, pitch) receive zero codes (loaded as zeros).
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (r0 + 16 < pitch) d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int64_t n_tiles = (rows + kTile - 1) / kTile;
+        scales[(b * n_tiles + r0 / kTile) * kAtomBytes + atom_offset(c, kb & 3)] = sb;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, int elem, int layout,
+                              uint8_t* codes, uint8_t* scales, int64_t rows_per_mat,
+                              cudaStream_t st) {
+    const int64_t total = lines * ((cols + 31) / 32);
+    if (total == 0) return cudaSuccess;
+    const int vec = (cols % 8 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(codes) & 15) == 0);
+    int dev = 0, nsm = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    blocks = blocks < static_cast<int64_t>(nsm) * 16 ? blocks : static_cast<int64_t>(nsm) * 16;
+    quant_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+        x, lines, cols, elem, layout, codes, scales, rows_per_mat > 0 ? rows_per_mat : lines, vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cols(const uint16_t* x, int64_t batch, int64_t rows, int64_t cols,
+                              int elem, int layout, uint8_t* codes, int64_t code_pitch,
+                              uint8_t* scales, cudaStream_t st) {
+    if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+    dim3 grid(static_cast<unsigned>((rows + 31) / 32),
+              static_cast<unsigned>((cols + kColTileC - 1) / kColTileC),
+              static_cast<unsigned>(batch));
+    quant_cols_kernel<<<grid, 256, 0, st>>>(x, rows, cols, elem, layout, codes, code_pitch, scales);
+    return cudaGetLastError();
+}
+
+}  // namespace fsa

@@ -1,0 +1,83 @@
+"""C-ABI library checks that need no GPU: the library loads, exports every
+symbol include/fsa.h declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import matrix_core_softmax_gb300 as fsa
+from matrix_core_softmax_gb300 import build as fsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fsa_build.build()
+    return fsa.load()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "fsa.h")).read()
+    return sorted(set(re.findall(r"FSA_API\s+[\w\s\*]+?\b(fsa_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(fsa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert fsa.status_string(s)
+    assert fsa.status_string(0) == "ok"
+
+
+def test_workspace_size(lib):
+    assert fsa.workspace_size(1, 2, 512, 64) > 3 * 2 * 512 * 64
+    assert lib.fsa_attention_workspace_size(1, 1, 100, 96, 0) == 0   # unsupported D
+    assert lib.fsa_attention_workspace_size(0, 1, 100, 64, 0) == 0
+    assert lib.fsa_attention_workspace_size(1, 1, 100, 64, 7) == 0
+
+
+def _attn(lib, q=16, k=16, v=16, o=16, B=1, H=1, S=8, D=64, fmt=0, theta=8.0):
+    P = ctypes.c_void_p
+    return lib.fsa_attention_fwd(P(q) if q else None, P(k) if k else None, P(v) if v else None,
+                                 P(o) if o else None, B, H, S, D, fmt, theta, None)
+
+
+def test_attention_argument_validation(lib):
+    assert _attn(lib, q=0) == 1
+    assert _attn(lib, o=0) == 1
+    assert _attn(lib, S=0) == 1
+    assert _attn(lib, B=-1) == 1
+    assert _attn(lib, D=96) == 2
+    assert _attn(lib, q=8) == 1                     # not 16-byte aligned
+    assert _attn(lib, fmt=3) == 1
+    assert _attn(lib, theta=float("nan")) == 1
+    assert _attn(lib, theta=-1.0) == 1
+    assert _attn(lib, theta=81.0) == 1
+    assert _attn(lib, B=300, H=300) == 1            # more than 65535 heads
+
+
+def test_bf16_attention_argument_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.fsa_bf16_attention_fwd(None, P(16), P(16), P(16), 1, 1, 8, 64, None) == 1
+    assert lib.fsa_bf16_attention_fwd(P(16), P(16), P(16), P(16), 1, 1, 8, 80, None) == 2
+
+
+def test_quantize_argument_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.fsa_quantize_mx(None, 1, 4, 4, 1, 0, P(16), P(16), None) == 1
+    assert lib.fsa_quantize_mx(P(16), 1, 4, 4, 2, 0, P(16), P(16), None) == 1
+    assert lib.fsa_quantize_mx(P(16), 1, 4, 4, 1, 3, P(16), P(16), None) == 1
+    assert lib.fsa_quantize_mx(P(16), -1, 4, 4, 1, 0, P(16), P(16), None) == 1
+    assert lib.fsa_quantize_mx(P(17), 1, 4, 4, 1, 0, P(16), P(16), None) == 1
+    # empty tensor: nothing to do, no device needed
+    assert lib.fsa_quantize_mx(P(16), 0, 4, 4, 1, 0, P(16), P(16), None) == 0
