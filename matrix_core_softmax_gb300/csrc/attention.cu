@@ -20,12 +20,17 @@
 //     rolls back: O and l are rescaled by exp(m_old - m_new) in TMEM and the
 //     reference moves to the tile maximum ("recovery procedure", paragraph 5).
 //
-// Work decomposition: one CTA per (128-row query tile, head); 6 warps:
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r;
-//   warp 4     TMA producer (Q once; K, V^T tiles through a 3-stage ring);
-//   warp 5     TMEM allocator and the single MMA-issuing thread.
-// S is double-buffered in TMEM so that QK^T of tile t+1 overlaps the
-// softmax of tile t; P is double-buffered in shared memory.
+// Work decomposition: one CTA per (128-row query tile, head); 10 warps:
+//   warps 0-3  softmax warpgroup 0: KV tiles 0, 2, 4, ... (S buffer 0, P buffer 0)
+//   warps 4-7  softmax warpgroup 1: KV tiles 1, 3, 5, ... (S buffer 1, P buffer 1)
+//              thread r of a warpgroup owns query row r = TMEM lane r; the
+//              frozen reference is handed from one warpgroup to the other
+//              after every tile (shared memory + mbarrier);
+//   warp 8     TMA producer (Q once; K, V^T tiles through a 3-stage ring);
+//   warp 9     TMEM allocator and the single MMA-issuing thread.
+// QK^T of tile t+1 runs while tile t is converted, and each scheduler holds
+// two softmax warps.  Each tile is read from TMEM twice: pass 1 takes the
+// 32-key block maxima/minima (gate, block scales), pass 2 converts.
 //
 // MMA operands are E4M3 bit patterns for all three formats: every E2M3 and
 // E2M1 value is exactly an E4M3 value, kind::mxf8f6f4 runs at one rate for
@@ -41,13 +46,15 @@ namespace fsa {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // 2 softmax warpgroups + loader warp + MMA warp
+constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kTileBytes = 128 * 128;  // one 128 x 128 byte operand tile
 constexpr uint32_t kTmemCols = 512;
 // TMEM column map
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColL = 384;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384;  // S1 = kColS0 + 128
 constexpr uint32_t kColSfQ = 416, kColSfK = 420 /* +4*(t&1) */, kColSfP = 428 /* +4*(u&1) */,
                    kColSfV = 436 /* +4*(u&1) */, kColSfOnes = 444;
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic holds rne(x) in its low bits
 
 struct __align__(1024) Smem {
     uint8_t q[kTileBytes];
@@ -60,6 +67,7 @@ struct __align__(1024) Smem {
     uint8_t v_sf[kStages][kAtomBytes];
     uint8_t p_sf[2][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
+    float m_ref[2][128];  // reference maximum handed from one warpgroup to the other
     uint64_t bar_q;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
@@ -67,11 +75,14 @@ struct __align__(1024) Smem {
     uint64_t s_free[2];
     uint64_t p_full[2];
     uint64_t p_free[2];  // PV of the tile that used P buffer i retired
+    uint64_t m_ready[2]; // warpgroup i published the reference after its tile
     uint64_t o_full;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+
+static_assert(sizeof(Smem) <= 232448, "shared memory beyond the 227 KB a CTA may use");
 
 struct Params {
     const uint8_t* q_sf;
@@ -114,22 +125,109 @@ __device__ __forceinline__ int p_scale_exp(uint32_t amax_bf16, int emax, uint32_
     return min(127, max(-127, X));
 }
 
-// Schraudolph code of one score: clamp(rne(alpha * s + beta), 0, 0x7F7F).
-// The clamp is applied in FP32 and 1.5 * 2^23 is added so that the integer
-// lands in the low mantissa bits (0x4B400000 has zero low 16 bits).
-__device__ __forceinline__ uint32_t schraudolph_code(float s, float alpha, float beta) {
-    float y = __fmaf_rn(s, alpha, beta);
-    y = fminf(fmaxf(y, 0.0f), 32639.0f);
-    return __float_as_uint(__fadd_rn(y, 12582912.0f)) & 0xFFFFu;
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max and min of 32 raw scores.
+__device__ __forceinline__ void maxmin32(const uint32_t (&v)[32], float& mx, float& mn) {
+    float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+    float b = fmin3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+    for (int j = 3; j < 31; j += 2) {
+        a = fmax3(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        b = fmin3(b, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+    }
+    mx = fmaxf(a, __uint_as_float(v[31]));
+    mn = fminf(b, __uint_as_float(v[31]));
+}
+
+// Keys at or beyond n_valid (relative to this 32-key chunk) become -inf.
+__device__ __forceinline__ void mask32(uint32_t (&v)[32], int n_valid) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j >= n_valid) v[j] = 0xFF800000u;
+}
+
+// Schraudolph code of a single score: rne(max(alpha * s + beta, 0)).  The
+// upper clamp at 0x7F7F is never active: a row's scores never pass its
+// reference by more than theta <= 80, so y <= 128 * (127 + 80 log2 e) - 7.
+__device__ __forceinline__ uint32_t code_of(float s, float alpha, float beta) {
+    const float y = fmaxf(__fmaf_rn(s, alpha, beta), 0.0f);
+    return __float_as_uint(__fadd_rn(y, kMagic)) & 0xFFFFu;
+}
+
+// Two-stage conversion of 32 scores of one 32-key block: bf16 weight code
+// (integer reinterpretation) -> E4M3 pattern of p * inv, inv = 2^-(X+off).
+// Writes 8 words, element i in byte i % 4 of word i / 4.
+template <bool kClamp>
+__device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, float beta,
+                                          float inv, uint32_t (&w)[8]) {
+    const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
+    const float2 m2 = make_float2(kMagic, kMagic), i2 = make_float2(inv, inv);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float2 y = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                              a2, b2);
+        if (kClamp) {
+            y.x = fmaxf(y.x, 0.0f);
+            y.y = fmaxf(y.y, 0.0f);
+        }
+        y = __fadd2_rn(y, m2);
+        const float2 pw = make_float2(__uint_as_float(__float_as_uint(y.x) << 16),
+                                      __uint_as_float(__float_as_uint(y.y) << 16));
+        const float2 q = __fmul2_rn(pw, i2);
+        const uint32_t e = cvt_e4m3x2(q.x, q.y);
+        if (i & 1)
+            w[i >> 1] |= e << 16;
+        else
+            w[i >> 1] = e;
+    }
+}
+
+// E4M3 P when every score of the 32-key block converts to an E4M3 normal
+// (p / 2^X >= 2^-6): then the E4M3 pattern of bf16(code) / 2^X is linear in
+// the integer code, rne((code - 128 X - 15360) / 16) -- 15360 = 120 << 7
+// re-biases the exponent from bf16 (127) to E4M3 (7) and the division drops
+// four of the seven mantissa bits with round-to-nearest-even.  Two FP32 adds
+// perform both roundings: + 1.5 * 2^23 rounds y to the integer code, then
+// + kx (= 1.5 * 2^27 - 1.5 * 2^23 - 15360 - 128 X, a multiple of 16) lands
+// in [2^27, 2^28) where one unit in the last place is 16, rounding the
+// quotient to nearest even; its low byte is the E4M3 code.
+__device__ __forceinline__ void convert32_linear(const uint32_t (&v)[32], float alpha, float beta,
+                                                 float kx, uint32_t (&w)[8]) {
+    const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
+    const float2 m2 = make_float2(kMagic, kMagic), k2 = make_float2(kx, kx);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float2 y0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), a2, b2);
+        float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), a2, b2);
+        y0 = __fadd2_rn(__fadd2_rn(y0, m2), k2);
+        y1 = __fadd2_rn(__fadd2_rn(y1, m2), k2);
+        const uint32_t lo = __byte_perm(__float_as_uint(y0.x), __float_as_uint(y0.y), 0x0040);
+        const uint32_t hi = __byte_perm(__float_as_uint(y1.x), __float_as_uint(y1.y), 0x0040);
+        w[i] = __byte_perm(lo, hi, 0x5410);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte-swizzled TMA/MMA tiles need a 1024-byte aligned base
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.err_word, kErrMisaligned);
+        return;
+    }
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -141,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkk = D / 32;  // MMA k-steps of the score product
 
     // ------------------------------------------------------------- setup
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -157,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.s_free[i], 128);
             mbar_init(&sm.p_full[i], 128);
             mbar_init(&sm.p_free[i], 1);
+            mbar_init(&sm.m_ready[i], 128);
         }
         mbar_init(&sm.o_full, 1);
         mbar_init(&sm.drain, 1);
@@ -173,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 4) {
+    if (warp == kWarpLoad) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -215,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t idesc_qk0 = idesc_mxf8f6f4(128, 128, 0, 0, 0, 0);
@@ -223,16 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_l0 = idesc_mxf8f6f4(128, 16, 0, 0, 0, 0);
             const uint32_t qk_swz = D == 128 ? SWZ_128B : SWZ_64B;
             const uint32_t qk_sbo = D == 128 ? 1024u : 512u;
-            const uint64_t sf_desc_q = smem_desc(smem_u32(sm.q_sf), 0, 128, SWZ_NONE);
             bool ok = mbar_wait(&sm.bar_q, 0, p.timeout_ns, &sm.abort);
             if (ok) {
                 tc_fence_after();
-                tc_cp_32x128b_x4(tmem + kColSfQ, sf_desc_q);
+                tc_cp_32x128b_x4(tmem + kColSfQ, smem_desc(smem_u32(sm.q_sf), 0, 128, SWZ_NONE));
                 tc_cp_32x128b_x4(tmem + kColSfOnes, smem_desc(smem_u32(sm.ones_sf), 0, 128, SWZ_NONE));
             }
-            auto issue_pv = [&](int u) -> bool {
+            auto issue_pv = [&](int u) {
                 const int pb = u & 1, st = u % kStages;
-                if (!mbar_wait(&sm.p_full[pb], (u >> 1) & 1, p.timeout_ns, &sm.abort)) return false;
                 tc_fence_after();
                 tc_cp_32x128b_x4(tmem + kColSfP + 4 * pb, smem_desc(smem_u32(sm.p_sf[pb]), 0, 128, SWZ_NONE));
                 tc_cp_32x128b_x4(tmem + kColSfV + 4 * pb, smem_desc(smem_u32(sm.v_sf[st]), 0, 128, SWZ_NONE));
@@ -256,26 +353,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(&sm.kv_empty[st]);
                 tc_commit(&sm.p_free[pb]);
-                return true;
             };
-            for (int t = 0; ok && t < p.n_t; ++t) {
-                const int st = t % kStages, sb = t & 1;
-                if (!mbar_wait(&sm.kv_full[st], (t / kStages) & 1, p.timeout_ns, &sm.abort)) { ok = false; break; }
-                if (t >= 2 && !mbar_wait(&sm.s_free[sb], ((t - 2) >> 1) & 1, p.timeout_ns, &sm.abort)) { ok = false; break; }
-                tc_fence_after();
-                tc_cp_32x128b_x4(tmem + kColSfK + 4 * sb, smem_desc(smem_u32(sm.k_sf[st]), 0, 128, SWZ_NONE));
-                for (int kk = 0; kk < nkk; ++kk) {
-                    const uint32_t sf = static_cast<uint32_t>(kk);
-                    const uint64_t ad = smem_desc(smem_u32(sm.q) + 32 * kk, 16, qk_sbo, qk_swz);
-                    const uint64_t bd = smem_desc(smem_u32(sm.k[st]) + 32 * kk, 16, qk_sbo, qk_swz);
-                    mma_mxf8f6f4(tmem + (sb ? kColS1 : kColS0), ad, bd,
-                                 idesc_qk0 | (sf << 4) | (sf << 29), tmem + kColSfQ,
-                                 tmem + kColSfK + 4 * sb, kk > 0 ? 1u : 0u);
+            // Issue order: a score product as soon as its K tile landed and its
+            // S buffer was released, ahead of any pending PV, so that a softmax
+            // warpgroup never waits behind the other warpgroup's P.  Each
+            // barrier below cannot complete its next phase before this thread
+            // issues the corresponding MMA, so the parities are unambiguous.
+            int qk = 0, pv = 0;
+            uint64_t idle_since = globaltimer_ns();
+            while (ok && pv < p.n_t) {
+                bool progressed = false;
+                if (qk < p.n_t) {
+                    const int st = qk % kStages, sb = qk & 1;
+                    if (mbar_test(&sm.kv_full[st], (qk / kStages) & 1) &&
+                        (qk < 2 || mbar_test(&sm.s_free[sb], ((qk - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        tc_cp_32x128b_x4(tmem + kColSfK + 4 * sb, smem_desc(smem_u32(sm.k_sf[st]), 0, 128, SWZ_NONE));
+                        for (int kk = 0; kk < nkk; ++kk) {
+                            const uint32_t sf = static_cast<uint32_t>(kk);
+                            const uint64_t ad = smem_desc(smem_u32(sm.q) + 32 * kk, 16, qk_sbo, qk_swz);
+                            const uint64_t bd = smem_desc(smem_u32(sm.k[st]) + 32 * kk, 16, qk_sbo, qk_swz);
+                            mma_mxf8f6f4(tmem + kColS0 + 128 * sb, ad, bd,
+                                         idesc_qk0 | (sf << 4) | (sf << 29), tmem + kColSfQ,
+                                         tmem + kColSfK + 4 * sb, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&sm.s_full[sb]);
+                        ++qk;
+                        progressed = true;
+                    }
                 }
-                tc_commit(&sm.s_full[sb]);
-                if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+                if (!progressed && pv < qk && mbar_test(&sm.p_full[pv & 1], (pv >> 1) & 1)) {
+                    issue_pv(pv);
+                    ++pv;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle_since = globaltimer_ns();
+                } else if (sm.abort || globaltimer_ns() - idle_since > p.timeout_ns) {
+                    ok = false;
+                } else {
+                    __nanosleep(32);  // leave the issue slots to the softmax warps
+                }
             }
-            if (ok && !issue_pv(p.n_t - 1)) ok = false;
             if (ok) tc_commit(&sm.o_full);
             if (!ok) {
                 raise_abort(sm, p);
@@ -286,74 +405,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------ softmax
-        const int r = tid;  // query row within the tile == TMEM lane
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // Warpgroup wg processes the KV tiles t = wg, wg + 2, ... in TMEM S
+        // buffer wg and shared P buffer wg; thread r owns query row r (TMEM
+        // lane r).  The reference maximum travels between the warpgroups
+        // through m_ref / m_ready after every tile.
+        const int wg = warp >> 2;
+        const int r = tid & 127;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = lane_addr + kColS0 + 128 * wg;
         const bool row_valid = (q0 + r) < p.S;
         const int64_t grow = static_cast<int64_t>(bh) * p.S + q0 + r;
-        float m_acc = 0.0f;  // frozen reference, accumulator units
-        float beta = 0.0f;
+        uint8_t* const prow = sm.p[wg] + (r >> 3) * 1024 + (r & 7) * 128;
+        float m_acc = 0.0f;  // reference maximum in accumulator units
         unsigned fired_total = 0;
         bool ok = true;
-        // PV_u retired.  p_free[u & 1] cannot run ahead of this thread: its
-        // next phase needs P of tile u + 2, which this thread has not written.
-        auto wait_pv = [&](int u) -> bool {
-            bool w = mbar_wait(&sm.p_free[u & 1], (u >> 1) & 1, p.timeout_ns, &sm.abort);
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool w = mbar_wait(bar, parity, p.timeout_ns, &sm.abort);
             return __all_sync(0xFFFFFFFFu, w);
         };
-        for (int t = 0; t < p.n_t; ++t) {
-            const int sb = t & 1;
-            bool w = mbar_wait(&sm.s_full[sb], (t >> 1) & 1, p.timeout_ns, &sm.abort);
-            if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+        for (int t = wg, it = 0; t < p.n_t; t += 2, ++it) {
+            if (!wait_all(&sm.s_full[wg], it & 1)) { ok = false; break; }
             tc_fence_after();
-            float s[128];
-            {
-                uint32_t rr[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(lane_addr + (sb ? kColS1 : kColS0) + 32 * c, rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(rr[j]);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.s_free[sb]);
-            // keys >= S are masked before the gate and the conversion
             const int n_valid = min(kTile, p.S - t * kTile);
-            if (n_valid < kTile) {
+            const bool tail = n_valid < kTile;
+            // pass 1: block maxima and minima of the raw scores
+            float bmax[4], bmin[4];
 #pragma unroll
-                for (int j = 0; j < 128; ++j)
-                    if (j >= n_valid) s[j] = -INFINITY;
-            }
-            float bmax[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                float mx = s[32 * b];
-#pragma unroll
-                for (int j = 1; j < 32; ++j) mx = fmaxf(mx, s[32 * b + j]);
-                bmax[b] = mx;
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(s_col + 64 * h, v0);
+                tmem_ld32(s_col + 64 * h + 32, v1);
+                tmem_ld_wait();
+                if (tail) {
+                    mask32(v0, n_valid - 64 * h);
+                    mask32(v1, n_valid - 64 * h - 32);
+                }
+                maxmin32(v0, bmax[2 * h], bmin[2 * h]);
+                maxmin32(v1, bmax[2 * h + 1], bmin[2 * h + 1]);
             }
             const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
+            // frozen reference: tile 0 sets it, the previous tile hands it on
+            if (t > 0) {
+                if (!wait_all(&sm.m_ready[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+                m_acc = sm.m_ref[wg ^ 1][r];
+            }
             bool fire = false;
             float rescale = 1.0f;
             if (t == 0) {
                 m_acc = tmax;
-                beta = 16249.0f - p.alpha * m_acc;
             } else if ((tmax - m_acc) * p.sm_scale > p.theta) {
                 fire = true;
                 rescale = expf((m_acc - tmax) * p.sm_scale);
                 m_acc = tmax;
-                beta = 16249.0f - p.alpha * m_acc;
             }
+            sm.m_ref[wg][r] = m_acc;
+            mbar_arrive(&sm.m_ready[wg]);
             if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
             fired_total += (fire && row_valid) ? 1u : 0u;
-            // P buffer sb is free once PV_{t-2} retired; a rollback needs PV_{t-1}
             const bool any_fire = __any_sync(0xFFFFFFFFu, fire);
-            if (any_fire && t >= 1 && !wait_pv(t - 1)) { ok = false; break; }
-            if (t >= 2 && !wait_pv(t - 2)) { ok = false; break; }
-            tc_fence_after();
             if (any_fire) {
-                // recovery: O and l of firing rows scaled by exp(m_old - m_new)
+                // recovery: once PV of the previous tile retired, O and l of the
+                // firing rows are scaled by exp(m_old - m_new) in TMEM
+                if (!wait_all(&sm.p_free[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
                 uint32_t rr[32];
                 for (int c = 0; c < D / 32; ++c) {
                     tmem_ld32(lane_addr + kColO + 32 * c, rr);
@@ -368,48 +482,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st1(lane_addr + kColL, __float_as_uint(__uint_as_float(lv) * rescale));
                 tmem_st_wait();
             }
-            // two-stage conversion: bf16 weight code -> MX P (E4M3 patterns)
-            uint8_t* prow = sm.p[sb] + (r >> 3) * 1024 + (r & 7) * 128;
+            // P buffer wg is free once PV of tile t - 2 retired
+            if (t >= 2 && !wait_all(&sm.p_free[wg], (it - 1) & 1)) { ok = false; break; }
+            const float beta = 16249.0f - p.alpha * m_acc;
+            // pass 2: per 32-key block, E8M0 scale from the block's largest
+            // weight code, then the conversion of its 32 scores
             uint32_t sfw = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const uint32_t cmax = schraudolph_code(bmax[b], p.alpha, beta);
-                const int X = p_scale_exp(cmax, p.p_emax, p.p_mthr);
-                const float inv = __int_as_float((127 - (X + p.p_off)) << 23);
-                sfw |= static_cast<uint32_t>(X + p.p_off + 127) << (8 * b);
-                uint32_t wv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t c0 = schraudolph_code(s[32 * b + 4 * i + 0], p.alpha, beta);
-                    uint32_t c1 = schraudolph_code(s[32 * b + 4 * i + 1], p.alpha, beta);
-                    uint32_t c2 = schraudolph_code(s[32 * b + 4 * i + 2], p.alpha, beta);
-                    uint32_t c3 = schraudolph_code(s[32 * b + 4 * i + 3], p.alpha, beta);
-                    uint32_t lo = cvt_e4m3x2(__uint_as_float(c0 << 16) * inv, __uint_as_float(c1 << 16) * inv);
-                    uint32_t hi = cvt_e4m3x2(__uint_as_float(c2 << 16) * inv, __uint_as_float(c3 << 16) * inv);
-                    wv[i] = (lo & 0xFFFFu) | (hi << 16);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(s_col + 64 * h, v0);
+                tmem_ld32(s_col + 64 * h + 32, v1);
+                tmem_ld_wait();
+                if (h == 1) {
+                    // the whole S tile has been read: release the buffer so the
+                    // next score product can start while this half converts
+                    tc_fence_before();
+                    mbar_arrive(&sm.s_free[wg]);
                 }
-                const int ch0 = 2 * b, ch1 = 2 * b + 1;  // 16-byte chunks of this block
-                *reinterpret_cast<uint4*>(prow + ((ch0 ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                *reinterpret_cast<uint4*>(prow + ((ch1 ^ (r & 7)) << 4)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                if (tail) {
+                    mask32(v0, n_valid - 64 * h);
+                    mask32(v1, n_valid - 64 * h - 32);
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int b = 2 * h + e;
+                    const float bx = h ? (e ? bmax[3] : bmax[2]) : (e ? bmax[1] : bmax[0]);
+                    const float bn = h ? (e ? bmin[3] : bmin[2]) : (e ? bmin[1] : bmin[0]);
+                    const int X = p_scale_exp(code_of(bx, p.alpha, beta), p.p_emax, p.p_mthr) + p.p_off;
+                    const float inv = __int_as_float((127 - X) << 23);
+                    sfw |= static_cast<uint32_t>(X + 127) << (8 * b);
+                    uint32_t w[8];
+                    // E4M3 P: the whole block converts to E4M3 normals when its
+                    // smallest code is a normal bf16 (>= 128) and at least
+                    // 128 X + 15488 (p / 2^X >= 2^-6)
+                    const bool linear = p.p_off == 0 &&
+                        __all_sync(0xFFFFFFFFu, static_cast<int>(code_of(bn, p.alpha, beta)) >= max(128, 128 * X + 15488));
+                    if (linear) {
+                        convert32_linear(e ? v1 : v0, p.alpha, beta,
+                                         static_cast<float>(188728320 - 128 * X), w);
+                    } else if (__any_sync(0xFFFFFFFFu, __fmaf_rn(bn, p.alpha, beta) < 0.0f)) {
+                        convert32<true>(e ? v1 : v0, p.alpha, beta, inv, w);
+                    } else {
+                        convert32<false>(e ? v1 : v0, p.alpha, beta, inv, w);
+                    }
+                    *reinterpret_cast<uint4*>(prow + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(prow + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             }
-            *reinterpret_cast<uint32_t*>(sm.p_sf[sb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
-            fence_async_smem();
             tc_fence_before();
-            mbar_arrive(&sm.p_full[sb]);
+            *reinterpret_cast<uint32_t*>(sm.p_sf[wg] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
+            fence_async_smem();
+            mbar_arrive(&sm.p_full[wg]);
         }
         if (!ok) raise_abort(sm, p);
         if (ok) {
-            bool w = mbar_wait(&sm.o_full, 0, p.timeout_ns, &sm.abort);
-            ok = __all_sync(0xFFFFFFFFu, w);
+            ok = wait_all(&sm.o_full, 0);
             if (!ok) raise_abort(sm, p);
         }
         if (ok) {
+            // epilogue: warpgroup wg writes columns [wg * D/2, (wg+1) * D/2)
             tc_fence_after();
             uint32_t lv;
             tmem_ld1(lane_addr + kColL, lv);
             tmem_ld_wait();
             const float l = __uint_as_float(lv);
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
                 uint32_t rr[32];
                 tmem_ld32(lane_addr + kColO + 32 * c, rr);
                 tmem_ld_wait();
@@ -439,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -468,7 +606,7 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.p_mthr = p_e4m3 ? 0x60u : 0x70u;
     p.timeout_ns = a.timeout_ns;
     p.debug_flags = a.debug_flags;
-    const size_t smem = sizeof(Smem) + 1024;
+    const size_t smem = sizeof(Smem);
     cudaError_t e = cudaFuncSetAttribute(fsa_attn_fwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -9,8 +9,8 @@
 // rescaled by exp2(m_old - m_new) whenever a row's maximum grows.
 //
 // Same decomposition as the MX kernel: one CTA per (128-row query tile,
-// head), warps 0-3 softmax (thread = row = TMEM lane), warp 4 TMA producer,
-// warp 5 TMEM allocator + MMA issuer.  Q and K are K-major (128-byte
+// head); two softmax warpgroups take alternate KV tiles (thread = row = TMEM
+// lane), warp 8 is the TMA producer, warp 9 the TMEM allocator + MMA issuer.  Q and K are K-major (128-byte
 // swizzle, 64 bf16 per swizzle row); V is read in its natural [keys][D]
 // layout as an MN-major B operand.
 #include <cuda_bf16.h>
@@ -22,29 +22,36 @@ namespace fsa {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // 2 softmax warpgroups + loader warp + MMA warp
+constexpr int kWarpLoad = 8, kWarpMma = 9;
 constexpr int kAtom = 128 * 128;         // 128 rows x 128 bytes (64 bf16)
 constexpr int kTileBytes = 2 * kAtom;    // 128 rows x 128 bf16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS0 = 0, kColO = 256;  // S1 = kColS0 + 128
 
 struct __align__(1024) Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint8_t p[kTileBytes];
+    uint8_t p[2][kTileBytes];
+    float m_run[2][128];   // running maximum handed between the warpgroups
+    float l_part[2][128];  // each warpgroup's final partial row sum (relative to m_run)
     uint64_t bar_q;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
     uint64_t s_free[2];
-    uint64_t p_full;
-    uint64_t p_free;
+    uint64_t p_full[2];
+    uint64_t p_free[2];
+    uint64_t m_ready[2];
+    uint64_t fin_ready;
     uint64_t o_full;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+
+static_assert(sizeof(Smem) <= 232448, "shared memory beyond the 227 KB a CTA may use");
 
 struct Params {
     __nv_bfloat16* o;
@@ -59,19 +66,42 @@ __device__ __forceinline__ void raise_abort(Smem& sm, const Params& p) {
     atomicOr(p.err_word, kErrTimeout);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float max32(const uint32_t (&v)[32]) {
+    float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+    for (int j = 3; j < 31; j += 2) a = fmax3(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+    return fmaxf(a, __uint_as_float(v[31]));
+}
+
+__device__ __forceinline__ void mask32(uint32_t (&v)[32], int n_valid) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j >= n_valid) v[j] = 0xFF800000u;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     bf16_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                        ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte-swizzled TMA/MMA tiles need a 1024-byte aligned base
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.err_word, kErrMisaligned);
+        return;
+    }
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q0 = blockIdx.x * kTile, bh = blockIdx.y;
     const int D = p.D;
     const int n_atoms = D / 64;  // swizzle atoms along D
 
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -85,9 +115,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_free[i], 128);
+            mbar_init(&sm.p_full[i], 128);
+            mbar_init(&sm.p_free[i], 1);
+            mbar_init(&sm.m_ready[i], 128);
         }
-        mbar_init(&sm.p_full, 128);
-        mbar_init(&sm.p_free, 1);
+        mbar_init(&sm.fin_ready, 256);
+        for (int i = 0; i < 256; ++i) {
+            (&sm.m_run[0][0])[i] = -INFINITY;
+            (&sm.l_part[0][0])[i] = 0.0f;
+        }
         mbar_init(&sm.o_full, 1);
         mbar_init(&sm.drain, 1);
         fence_mbar_init();
@@ -97,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 4) {
+    if (warp == kWarpLoad) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -129,25 +165,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, p.timeout_ns, &dummy);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
             const uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);
             bool ok = mbar_wait(&sm.bar_q, 0, p.timeout_ns, &sm.abort);
             auto issue_pv = [&](int u) -> bool {
-                const int st = u % kStages;
-                if (!mbar_wait(&sm.p_full, u & 1, p.timeout_ns, &sm.abort)) return false;
+                const int st = u % kStages, pb = u & 1;
+                if (!mbar_wait(&sm.p_full[pb], (u >> 1) & 1, p.timeout_ns, &sm.abort)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-                    const uint64_t ad = smem_desc(smem_u32(sm.p) + (kk >> 2) * kAtom + 32 * (kk & 3), 16,
+                    const uint64_t ad = smem_desc(smem_u32(sm.p[pb]) + (kk >> 2) * kAtom + 32 * (kk & 3), 16,
                                                   1024, SWZ_128B);
                     // V: MN-major; 64-wide d atoms kAtom apart (LBO), 8-key groups 1024 apart (SBO)
                     const uint64_t bd = smem_desc(smem_u32(sm.v[st]) + kk * 16 * 128, kAtom, 1024, SWZ_128B);
                     mma_bf16(tmem + kColO, ad, bd, idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&sm.kv_empty[st]);
-                tc_commit(&sm.p_free);
+                tc_commit(&sm.p_free[pb]);
                 return true;
             };
             for (int t = 0; ok && t < p.n_t; ++t) {
@@ -159,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = (kk >> 2) * kAtom + 32 * (kk & 3);
                     const uint64_t ad = smem_desc(smem_u32(sm.q) + off, 16, 1024, SWZ_128B);
                     const uint64_t bd = smem_desc(smem_u32(sm.k[st]) + off, 16, 1024, SWZ_128B);
-                    mma_bf16(tmem + (sb ? kColS1 : kColS0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + kColS0 + 128 * sb, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&sm.s_full[sb]);
                 if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
@@ -174,94 +210,127 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        const int r = tid;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // softmax warpgroup wg: KV tiles wg, wg + 2, ...; thread r = row r.
+        // The running maximum is handed between the warpgroups after every
+        // tile; each warpgroup keeps its own partial row sum relative to the
+        // maximum of its latest tile, combined at the end.
+        const int wg = warp >> 2;
+        const int r = tid & 127;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = lane_addr + kColS0 + 128 * wg;
         const bool row_valid = (q0 + r) < p.S;
         const int64_t grow = static_cast<int64_t>(bh) * p.S + q0 + r;
         float m = -INFINITY;  // running max of s * c
-        float l = 0.0f;
+        float l = 0.0f;       // this warpgroup's partial sum, relative to m
         bool ok = true;
-        for (int t = 0; t < p.n_t; ++t) {
-            const int sb = t & 1;
-            bool w = mbar_wait(&sm.s_full[sb], (t >> 1) & 1, p.timeout_ns, &sm.abort);
-            if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            const bool w = mbar_wait(bar, parity, p.timeout_ns, &sm.abort);
+            return __all_sync(0xFFFFFFFFu, w);
+        };
+        for (int t = wg, it = 0; t < p.n_t; t += 2, ++it) {
+            if (!wait_all(&sm.s_full[wg], it & 1)) { ok = false; break; }
             tc_fence_after();
-            float x[128];
-            {
-                uint32_t rr[32];
+            const int n_valid = min(kTile, p.S - t * kTile);
+            const bool tail = n_valid < kTile;
+            float tmax = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(lane_addr + (sb ? kColS1 : kColS0) + 32 * c, rr);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(s_col + 64 * h, v0);
+                tmem_ld32(s_col + 64 * h + 32, v1);
+                tmem_ld_wait();
+                if (tail) {
+                    mask32(v0, n_valid - 64 * h);
+                    mask32(v1, n_valid - 64 * h - 32);
+                }
+                tmax = fmax3(tmax, max32(v0), max32(v1));
+            }
+            float m_prev = m;
+            if (t > 0) {
+                if (!wait_all(&sm.m_ready[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+                m_prev = sm.m_run[wg ^ 1][r];
+            }
+            const float m_new = fmaxf(m_prev, tmax * p.c);
+            sm.m_run[wg][r] = m_new;
+            mbar_arrive(&sm.m_ready[wg]);
+            // O (all tiles so far) is relative to m_prev; rescale when it grew
+            const bool grew = m_new > m_prev;
+            if (t >= 1 && __any_sync(0xFFFFFFFFu, grew)) {
+                if (!wait_all(&sm.p_free[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const float corr = exp2f(m_prev - m_new);
+                uint32_t rr[32];
+                for (int c = 0; c < D / 32; ++c) {
+                    tmem_ld32(lane_addr + kColO + 32 * c, rr);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[32 * c + j] = __uint_as_float(rr[j]) * p.c;
+                    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * corr);
+                    tmem_st32(lane_addr + kColO + 32 * c, rr);
                 }
+                tmem_st_wait();
             }
-            tc_fence_before();
-            mbar_arrive(&sm.s_free[sb]);
-            const int n_valid = min(kTile, p.S - t * kTile);
-            if (n_valid < kTile) {
-#pragma unroll
-                for (int j = 0; j < 128; ++j)
-                    if (j >= n_valid) x[j] = -INFINITY;
-            }
-            float mx = m;
-#pragma unroll
-            for (int j = 0; j < 128; ++j) mx = fmaxf(mx, x[j]);
-            const float corr = exp2f(m - mx);  // 0 on the first tile (m = -inf)
-            const bool grew = mx > m;
-            m = mx;
+            if (t >= 2 && !wait_all(&sm.p_free[wg], (it - 1) & 1)) { ok = false; break; }
+            // own partial sum follows the new maximum
+            l = (m == -INFINITY) ? 0.0f : l * exp2f(m - m_new);
+            m = m_new;
             float ls = 0.0f;
-            uint32_t pk[64];
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(s_col + 64 * h, v0);
+                tmem_ld32(s_col + 64 * h + 32, v1);
+                tmem_ld_wait();
+                if (tail) {
+                    mask32(v0, n_valid - 64 * h);
+                    mask32(v1, n_valid - 64 * h - 32);
+                }
+                uint8_t* prow = sm.p[wg] + h * kAtom + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float a = exp2f(x[2 * j] - m), b = exp2f(x[2 * j + 1] - m);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-                ls += __low2float(h2) + __high2float(h2);
-                pk[j] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            l = l * corr + ls;
-            // O must have absorbed PV_{t-1} before it is rescaled or P is overwritten
-            if (t >= 1) {
-                bool w2 = mbar_wait(&sm.p_free, (t - 1) & 1, p.timeout_ns, &sm.abort);
-                if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, grew)) {
-                    uint32_t rr[32];
-                    for (int c = 0; c < D / 32; ++c) {
-                        tmem_ld32(lane_addr + kColO + 32 * c, rr);
-                        tmem_ld_wait();
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t pk[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * corr);
-                        tmem_st32(lane_addr + kColO + 32 * c, rr);
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t* v = e ? v1 : v0;
+                        const float a = exp2f(__fmaf_rn(__uint_as_float(v[2 * j]), p.c, -m));
+                        const float b = exp2f(__fmaf_rn(__uint_as_float(v[2 * j + 1]), p.c, -m));
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+                        ls += __low2float(h2) + __high2float(h2);
+                        pk[j] = *reinterpret_cast<uint32_t*>(&h2);
                     }
-                    tmem_st_wait();
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const int c = 4 * e + ch;  // 16-byte chunk within the 128-byte row
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                    }
                 }
             }
-            // P row r: two 64-key swizzle atoms of 128 bytes
-#pragma unroll
-            for (int a = 0; a < 2; ++a) {
-                uint8_t* prow = sm.p + a * kAtom + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int j = a * 32 + ch * 4;
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-                        make_uint4(pk[j], pk[j + 1], pk[j + 2], pk[j + 3]);
-                }
-            }
-            fence_async_smem();
+            l += ls;
             tc_fence_before();
-            mbar_arrive(&sm.p_full);
+            mbar_arrive(&sm.s_free[wg]);
+            fence_async_smem();
+            mbar_arrive(&sm.p_full[wg]);
         }
         if (!ok) raise_abort(sm, p);
+        // combine the two partial sums: l = sum_w l_w * 2^(m_w - m_final)
         if (ok) {
-            bool w = mbar_wait(&sm.o_full, 0, p.timeout_ns, &sm.abort);
-            ok = __all_sync(0xFFFFFFFFu, w);
+            sm.l_part[wg][r] = l;
+            mbar_arrive(&sm.fin_ready);
+            ok = wait_all(&sm.fin_ready, 0);
             if (!ok) raise_abort(sm, p);
         }
         if (ok) {
+            ok = wait_all(&sm.o_full, 0);
+            if (!ok) raise_abort(sm, p);
+        }
+        if (ok) {
+            const float m0 = sm.m_run[0][r], l0 = sm.l_part[0][r];
+            const float m1 = sm.m_run[1][r], l1 = sm.l_part[1][r];
+            const float mf = fmaxf(m0, m1);
+            const float lt = (m0 == -INFINITY ? 0.0f : l0 * exp2f(m0 - mf)) +
+                             (m1 == -INFINITY ? 0.0f : l1 * exp2f(m1 - mf));
             tc_fence_after();
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
                 uint32_t rr[32];
                 tmem_ld32(lane_addr + kColO + 32 * c, rr);
                 tmem_ld_wait();
@@ -269,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * j]), l),
-                                                                  __fdiv_rn(__uint_as_float(rr[2 * j + 1]), l));
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * j]), lt),
+                                                                  __fdiv_rn(__uint_as_float(rr[2 * j + 1]), lt));
                         packed[j] = *reinterpret_cast<uint32_t*>(&h2);
                     }
                     uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + 32 * c);
@@ -284,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -301,7 +370,7 @@ cudaError_t launch_bf16_attention(const Bf16Launch& a, cudaStream_t st) {
     p.n_t = (a.S + kTile - 1) / kTile;
     p.c = static_cast<float>(static_cast<double>(a.sm_scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
-    const size_t smem = sizeof(Smem) + 1024;
+    const size_t smem = sizeof(Smem);
     cudaError_t e = cudaFuncSetAttribute(bf16_attn_fwd_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -389,7 +389,8 @@ fsa_status fsa_get_device_error(void* stream) {
         if (cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return FSA_ERR_CUDA;
     }
-    return (w & kErrTimeout) ? FSA_ERR_TIMEOUT : FSA_OK;
+    if (w & kErrTimeout) return FSA_ERR_TIMEOUT;
+    return w ? FSA_ERR_CUDA : FSA_OK;
 }
 
 void fsa_release_workspace(void) {

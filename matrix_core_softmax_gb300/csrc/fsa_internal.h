@@ -75,5 +75,6 @@ cudaError_t launch_bf16_attention(const Bf16Launch& a, cudaStream_t st);
 
 // Device error word codes.
 constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrMisaligned = 2u;  // shared-memory base not 1024-byte aligned
 
 }  // namespace fsa

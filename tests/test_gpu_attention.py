@@ -147,3 +147,33 @@ def test_bounded_wait_reports_timeout_and_context_survives(fsa):
     assert fsa.get_device_error() == 0
     ref = oracle.attention(q, k, v, fmt="mxfp8", mode="fused")["out"]
     assert oracle.rel_l2(to_f64(o).reshape(-1, D), ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp6", "mxfp4"])
+@pytest.mark.parametrize("qscale", [16.0, 0.02])
+def test_fused_wide_and_narrow_score_ranges(fsa, fmt, qscale):
+    # q x 16: scores spread over hundreds of natural-log units, so weights
+    # underflow (clamped codes, subnormal P blocks); q x 0.02: nearly flat rows
+    B, H, S, D = 1, 2, 600, 128
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=21)
+    q = fsa_inputs.to_bf16_bits(fsa_inputs.bf16_bits_to_f32(q) * np.float32(qscale))
+    o, _, _ = _run(fsa, q, k, v, fmt, theta=80.0)
+    ref = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=80.0)["out"]
+    got = to_f64(o).reshape(-1, D)
+    assert np.all(np.isfinite(got))
+    assert oracle.rel_l2(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_gate_at_theta_zero(fsa, fmt):
+    # theta = 0: every tile whose max passes the reference rolls back
+    B, H, S, D = 1, 2, 1500, 64
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=22)
+    o, rb, cnt = _run(fsa, q, k, v, fmt, theta=0.0, want_bits=True)
+    r = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=0.0, want_bits=True,
+                         want_margins=True)
+    bits = rb.cpu().numpy()
+    near = np.abs(np.nan_to_num(r["margins"], nan=1.0)) < NEAR_TIE
+    assert r["rollback_count"] > 100
+    assert np.array_equal(bits[~near], r["bits"][~near])
+    assert oracle.rel_l2(to_f64(o).reshape(-1, D), r["out"]) <= TOL
