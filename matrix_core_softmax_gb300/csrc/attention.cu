@@ -14,20 +14,22 @@
 //     reinterpretation); each 32-key block of those bf16 weights gets its
 //     E8M0 scale and is converted to the P element type (two-stage
 //     conversion);
-//   * O += P^ V^ and l += P^ 1 are two more block-scaled MMAs on the same
-//     P^ in shared memory (l uses a 16-column all-ones B operand);
+//   * O += P^ V^ and l += P^ 1 come from one more block-scaled MMA on the
+//     same P^ in shared memory: the V^T operand carries 16 extra all-ones
+//     rows, so column D of the accumulator is the row sum;
 //   * a row whose tile maximum passes its reference by more than theta
 //     rolls back: O and l are rescaled by exp(m_old - m_new) in TMEM and the
 //     reference moves to the tile maximum ("recovery procedure", paragraph 5).
 //
 // Work decomposition: one CTA per (128-row query tile, head); 10 warps:
-//   warps 0-3  softmax warpgroup 0: KV tiles 0, 2, 4, ... (S buffer 0, P buffer 0)
-//   warps 4-7  softmax warpgroup 1: KV tiles 1, 3, 5, ... (S buffer 1, P buffer 1)
+//   warps 0-3  softmax warpgroup 0: KV tiles 0, 2, 4, ... (S buffer 0, P buffers 0, 2)
+//   warps 4-7  softmax warpgroup 1: KV tiles 1, 3, 5, ... (S buffer 1, P buffers 1, 3)
 //              thread r of a warpgroup owns query row r = TMEM lane r; the
 //              frozen reference is handed from one warpgroup to the other
 //              after every tile (shared memory + mbarrier);
-//   warp 8     TMA producer (Q once; K, V^T tiles through a 3-stage ring);
-//   warp 9     TMEM allocator and the single MMA-issuing thread.
+//   warp 8     TMA producer of Q and the K ring; warp 10 of the V^T ring;
+//   warp 9     TMEM allocator and issuer of the score products;
+//   warp 11    issuer of the PV products (four P buffers in shared memory).
 // QK^T of tile t+1 runs while tile t is converted, and each scheduler holds
 // two softmax warps.  Each tile is read from TMEM twice: pass 1 takes the
 // 32-key block maxima/minima (gate, block scales), pass 2 converts.
@@ -46,38 +48,48 @@ namespace fsa {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 320;          // 2 softmax warpgroups + loader warp + MMA warp
-constexpr int kWarpLoad = 8, kWarpMma = 9;
+constexpr int kPBuf = 4;  // P buffers: tile t uses t % 4 (two per warpgroup)
+constexpr int kThreads = 384;  // 2 softmax warpgroups + (K loader, MMA, V loader, spare)
+constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpLoadV = 10, kWarpPv = 11;
+// Register split: launched at 168 per thread (384 x 168 = 64512), the helper
+// warpgroup gives back to 48 and the softmax warpgroups take 224:
+// 2 * 128 * 224 + 128 * 48 = 63488 <= 64512.
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 224, kHelperRegs = 48;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kTileBytes = 128 * 128;  // one 128 x 128 byte operand tile
+constexpr int kVBytes = kTileBytes + 16 * 128;  // V^T tile + 16 all-ones rows (row sums)
 constexpr uint32_t kTmemCols = 512;
-// TMEM column map
-constexpr uint32_t kColS0 = 0, kColO = 256, kColL = 384;  // S1 = kColS0 + 128
-constexpr uint32_t kColSfQ = 416, kColSfK = 420 /* +4*(t&1) */, kColSfP = 428 /* +4*(u&1) */,
-                   kColSfV = 436 /* +4*(u&1) */, kColSfOnes = 444;
+// TMEM column map: S0, S1 (128 each), O (D columns) with l in column D of
+// the same accumulator, and the scale-factor atoms (4 columns per atom)
+constexpr uint32_t kColS0 = 0, kColO = 256;  // S1 = kColS0 + 128, l = kColO + D
+constexpr uint32_t kColSfQ = 416, kColSfK = 420 /* +4*(t&1) */, kColSfP = 428 /* +4*(t%4) */,
+                   kColSfV = 444 /* +8*(u&1): V rows 0-127, then unit scales for rows 128-255 */;
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic holds rne(x) in its low bits
 
 struct __align__(1024) Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
-    uint8_t v[kStages][kTileBytes];
-    uint8_t p[2][kTileBytes];
-    uint8_t ones[16 * 128];
+    uint8_t v[kStages][kVBytes];  // rows [0, D): V^T tile; rows [D, D+16): all ones
+    uint8_t p[kPBuf][kTileBytes];
     uint8_t q_sf[kAtomBytes];
     uint8_t k_sf[kStages][kAtomBytes];
     uint8_t v_sf[kStages][kAtomBytes];
-    uint8_t p_sf[2][kAtomBytes];
+    uint8_t p_sf[kPBuf][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
     float m_ref[2][128];  // reference maximum handed from one warpgroup to the other
     uint64_t bar_q;
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
+    uint64_t k_full[kStages];   // K tile landed
+    uint64_t k_empty[kStages];  // score product that read the K tile retired
+    uint64_t v_full[kStages];
+    uint64_t v_empty[kStages];  // PV product that read the V tile retired
     uint64_t s_full[2];
     uint64_t s_free[2];
-    uint64_t p_full[2];
-    uint64_t p_free[2];  // PV of the tile that used P buffer i retired
+    uint64_t p_full[kPBuf];
+    uint64_t p_free[kPBuf];  // PV of the tile that used P buffer i retired
     uint64_t m_ready[2]; // warpgroup i published the reference after its tile
     uint64_t o_full;
-    uint64_t drain;
+    uint64_t drain_qk, drain_pv;
     uint32_t tmem_base;
     int abort;
 };
@@ -96,9 +108,6 @@ struct Params {
     float sm_scale;  // s = sm_scale * accumulator
     float alpha;     // 128 * log2(e) * sm_scale
     float theta;     // gate threshold, natural-log score units
-    int p_off;       // 0: P in E4M3; 6: P on the E2M3 grid
-    int p_emax;      // largest exponent of the P element type
-    uint32_t p_mthr; // its largest mantissa in bf16 units
     uint64_t timeout_ns;
     int debug_flags;
 };
@@ -136,17 +145,21 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
     return d;
 }
 
-// Max and min of 32 raw scores.
+// Max and min of 32 raw scores (three-input max/min in a depth-4 tree, so the
+// reductions do not serialise on instruction latency).
 __device__ __forceinline__ void maxmin32(const uint32_t (&v)[32], float& mx, float& mn) {
-    float a = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-    float b = fmin3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+    float a[11], b[11];
 #pragma unroll
-    for (int j = 3; j < 31; j += 2) {
-        a = fmax3(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-        b = fmin3(b, __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+    for (int i = 0; i < 10; ++i) {
+        a[i] = fmax3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
+        b[i] = fmin3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
     }
-    mx = fmaxf(a, __uint_as_float(v[31]));
-    mn = fminf(b, __uint_as_float(v[31]));
+    a[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+    b[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+    const float a0 = fmax3(a[0], a[1], a[2]), a1 = fmax3(a[3], a[4], a[5]), a2 = fmax3(a[6], a[7], a[8]);
+    const float b0 = fmin3(b[0], b[1], b[2]), b1 = fmin3(b[3], b[4], b[5]), b2 = fmin3(b[6], b[7], b[8]);
+    mx = fmax3(fmax3(a0, a1, a2), a[9], a[10]);
+    mn = fmin3(fmin3(b0, b1, b2), b[9], b[10]);
 }
 
 // Keys at or beyond n_valid (relative to this 32-key chunk) become -inf.
@@ -217,6 +230,152 @@ __device__ __forceinline__ void convert32_linear(const uint32_t (&v)[32], float 
     }
 }
 
+// P element type: E4M3 (MXFP8) or six-bit E2M3 (MXFP6, MXFP4) stored as the
+// E4M3 pattern of p / 2^(X+6).  emax / mthr describe the largest element
+// (1 + mthr/128) * 2^emax for the scale rule.
+template <bool kE4M3> struct PType;
+template <> struct PType<true> { static constexpr int kOff = 0, kEmax = 8; static constexpr uint32_t kMthr = 0x60; };
+template <> struct PType<false> { static constexpr int kOff = 6, kEmax = 2; static constexpr uint32_t kMthr = 0x70; };
+
+// Pass 2 for one 32-key block b of row r: the block's E8M0 scale from its
+// largest weight code, the conversion of its 32 scores, and the two 16-byte
+// stores into the 128-byte-swizzled P row.  Returns the scale byte.
+template <bool kE4M3>
+__device__ __forceinline__ uint32_t convert_block(const uint32_t (&v)[32], int b, float bx, float bn,
+                                                  float alpha, float beta, uint8_t* prow, int r) {
+    using T = PType<kE4M3>;
+    const int X = p_scale_exp(code_of(bx, alpha, beta), T::kEmax, T::kMthr) + T::kOff;
+    const float inv = __int_as_float((127 - X) << 23);
+    uint32_t w[8];
+    if (kE4M3) {
+        // the whole block converts to E4M3 normals when its smallest code is a
+        // normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6)
+        if (__all_sync(0xFFFFFFFFu,
+                       static_cast<int>(code_of(bn, alpha, beta)) >= max(128, 128 * X + 15488))) {
+            // kx = 188728320 - 128 X; one unit of X is 8 units in the last
+            // place of a float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f
+            convert32_linear(v, alpha, beta, __int_as_float(0x4D33FC40 - 8 * X), w);
+        } else {
+            convert32<true>(v, alpha, beta, inv, w);
+        }
+    } else {
+        if (__any_sync(0xFFFFFFFFu, __fmaf_rn(bn, alpha, beta) < 0.0f))
+            convert32<true>(v, alpha, beta, inv, w);
+        else
+            convert32<false>(v, alpha, beta, inv, w);
+    }
+    *reinterpret_cast<uint4*>(prow + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(prow + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    return static_cast<uint32_t>(X + 127);
+}
+
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Params& p, Smem& sm) {
+    const bool w = mbar_wait(bar, parity, p.timeout_ns, &sm.abort);
+    return __all_sync(0xFFFFFFFFu, w);
+}
+
+// Per-row state of a softmax thread.
+struct RowState {
+    float m_acc;          // frozen reference, accumulator units
+    unsigned fired;       // gate firings of this row
+};
+
+// One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
+// scores once (one TMEM wait), release the S buffer, block max/min, the
+// reference hand-off and the gate (with the O / l rescale on a rollback),
+// then the two-stage conversion into P buffer wg.  false = aborted.
+template <bool kE4M3, bool kTail>
+__device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
+                                             int r, uint32_t lane_addr, uint32_t s_col,
+                                             bool row_valid, int64_t grow, RowState& rs) {
+    const int D = p.D;
+    const int pb = t & (kPBuf - 1);
+    uint8_t* const prow = sm.p[pb] + (r >> 3) * 1024 + (r & 7) * 128;
+    if (!wait_warp(&sm.s_full[wg], it & 1, p, sm)) return false;
+    tc_fence_after();
+    uint32_t s0[32], s1[32], s2[32], s3[32];
+    tmem_ld32(s_col, s0);
+    tmem_ld32(s_col + 32, s1);
+    tmem_ld32(s_col + 64, s2);
+    tmem_ld32(s_col + 96, s3);
+    tmem_ld_wait();
+    tmem_reg_dep(s0);
+    tmem_reg_dep(s1);
+    tmem_reg_dep(s2);
+    tmem_reg_dep(s3);
+    // the whole tile is in registers: the next score product may reuse S
+    tc_fence_before();
+    mbar_arrive(&sm.s_free[wg]);
+    if (kTail) {
+        // keys >= S are masked before the gate and the conversion
+        const int n_valid = p.S - t * kTile;
+        mask32(s0, n_valid);
+        mask32(s1, n_valid - 32);
+        mask32(s2, n_valid - 64);
+        mask32(s3, n_valid - 96);
+    }
+    float bmax[4], bmin[4];
+    maxmin32(s0, bmax[0], bmin[0]);
+    maxmin32(s1, bmax[1], bmin[1]);
+    maxmin32(s2, bmax[2], bmin[2]);
+    maxmin32(s3, bmax[3], bmin[3]);
+    const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
+    // frozen reference: tile 0 sets it, the previous tile hands it on
+    if (t > 0) {
+        if (!wait_warp(&sm.m_ready[wg ^ 1], ((t - 1) >> 1) & 1, p, sm)) return false;
+        rs.m_acc = sm.m_ref[wg ^ 1][r];
+    }
+    bool fire = false;
+    float rescale = 1.0f;
+    if (t == 0) {
+        rs.m_acc = tmax;
+    } else if ((tmax - rs.m_acc) * p.sm_scale > p.theta) {
+        fire = true;
+        rescale = expf((rs.m_acc - tmax) * p.sm_scale);
+        rs.m_acc = tmax;
+    }
+    sm.m_ref[wg][r] = rs.m_acc;
+    mbar_arrive(&sm.m_ready[wg]);
+    if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
+    rs.fired += (fire && row_valid) ? 1u : 0u;
+    // P buffer pb is free once PV of tile t - 4 retired.  Waited first: PV
+    // products retire in order, so afterwards the barrier of tile t - 1's
+    // buffer can only be in the phase of PV_{t-1} itself.
+    if (t >= kPBuf && !wait_warp(&sm.p_free[pb], ((t / kPBuf) - 1) & 1, p, sm)) return false;
+    if (__any_sync(0xFFFFFFFFu, fire)) {
+        // recovery: once PV of the previous tile retired, O and l of the
+        // firing rows are scaled by exp(m_old - m_new) in TMEM
+        const int pp = (t - 1) & (kPBuf - 1);
+        if (!wait_warp(&sm.p_free[pp], ((t - 1) / kPBuf) & 1, p, sm)) return false;
+        tc_fence_after();
+        uint32_t rr[32];
+        for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(lane_addr + kColO + 32 * c, rr);
+            tmem_ld_wait();
+            tmem_reg_dep(rr);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * rescale);
+            tmem_st32(lane_addr + kColO + 32 * c, rr);
+        }
+        uint32_t lv;
+        tmem_ld1(lane_addr + kColO + D, lv);
+        tmem_ld_wait();
+        tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
+        tmem_st_wait();
+    }
+    const float beta = 16249.0f - p.alpha * rs.m_acc;
+    uint32_t sfw = convert_block<kE4M3>(s0, 0, bmax[0], bmin[0], p.alpha, beta, prow, r);
+    sfw |= convert_block<kE4M3>(s1, 1, bmax[1], bmin[1], p.alpha, beta, prow, r) << 8;
+    sfw |= convert_block<kE4M3>(s2, 2, bmax[2], bmin[2], p.alpha, beta, prow, r) << 16;
+    sfw |= convert_block<kE4M3>(s3, 3, bmax[3], bmin[3], p.alpha, beta, prow, r) << 24;
+    tc_fence_before();
+    *reinterpret_cast<uint32_t*>(sm.p_sf[pb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
+    fence_async_smem();
+    mbar_arrive(&sm.p_full[pb]);
+    return true;
+}
+
+template <bool kE4M3>
 __global__ void __launch_bounds__(kThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -247,23 +406,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.abort = 0;
         mbar_init(&sm.bar_q, 1);
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.s_free[i], 128);
-            mbar_init(&sm.p_full[i], 128);
-            mbar_init(&sm.p_free[i], 1);
             mbar_init(&sm.m_ready[i], 128);
         }
+        for (int i = 0; i < kPBuf; ++i) {
+            mbar_init(&sm.p_full[i], 128);
+            mbar_init(&sm.p_free[i], 1);
+        }
         mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain_qk, 1);
+        mbar_init(&sm.drain_pv, 1);
         fence_mbar_init();
     }
     if (tid < 128) {
-        // all-ones B operand (E4M3 1.0 = 0x38) and unit scales (2^0 = 127)
-        reinterpret_cast<uint4*>(sm.ones)[tid] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        // 16 all-ones rows (E4M3 1.0 = 0x38) after the D rows of every V^T
+        // stage, so that one PV product of N = D + 16 also yields l = P 1,
+        // and a unit-scale atom (2^0 = 127) for those rows
+        for (int st = 0; st < kStages; ++st)
+            reinterpret_cast<uint4*>(sm.v[st] + p.D * 128)[tid] =
+                make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
         reinterpret_cast<uint32_t*>(sm.ones_sf)[tid] = 0x7F7F7F7Fu;
         fence_async_smem();
     }
@@ -272,138 +440,156 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == kWarpLoad) {
-        // ------------------------------------------------------ producer
+    if (warp == kWarpLoad || warp == kWarpLoadV) {
+        warpgroup_reg_dec<kHelperRegs>();
+        // ------------------------------------------------------ producers
+        // warp 8 loads Q once and the K ring, warp 10 the V^T ring; separate
+        // rings let K of tile t+3 load as soon as QK_t retired, long before
+        // PV_t releases V.
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
+            const bool is_k = warp == kWarpLoad;
             const uint32_t tile_bytes = static_cast<uint32_t>(kTile * D);
-            mbar_arrive_expect_tx(&sm.bar_q, tile_bytes + kAtomBytes);
-            tma_load_3d(sm.q, &tm_q, &sm.bar_q, 0, q0, bh);
-            bulk_load(sm.q_sf, p.q_sf + (static_cast<int64_t>(bh) * n_qt + qt) * kAtomBytes,
-                      kAtomBytes, &sm.bar_q);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                mbar_arrive_expect_tx(&sm.bar_q, tile_bytes + kAtomBytes);
+                tma_load_3d(sm.q, &tm_q, &sm.bar_q, 0, q0, bh);
+                bulk_load(sm.q_sf, p.q_sf + (static_cast<int64_t>(bh) * n_qt + qt) * kAtomBytes,
+                          kAtomBytes, &sm.bar_q);
+            } else {
+                tma_prefetch_desc(&tm_v);
+            }
+            uint64_t* full = is_k ? sm.k_full : sm.v_full;
+            uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
             int issued = 0;
             bool ok = true;
             for (int t = 0; t < p.n_t; ++t) {
                 const int st = t % kStages;
-                if (t >= kStages) {
-                    if (!mbar_wait(&sm.kv_empty[st], ((t / kStages) - 1) & 1, p.timeout_ns,
-                                   &sm.abort)) {
-                        ok = false;
-                        break;
-                    }
+                if (t >= kStages &&
+                    !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, p.timeout_ns, &sm.abort)) {
+                    ok = false;
+                    break;
                 }
-                if ((p.debug_flags & 1) && t == 1) continue;  // test: tile 1 never arrives
-                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * tile_bytes + 2 * kAtomBytes);
-                tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, t * kTile, bh);
-                tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], t * kTile, 0, bh);
+                if (is_k && (p.debug_flags & 1) && t == 1) continue;  // test: K tile 1 never arrives
+                mbar_arrive_expect_tx(&full[st], tile_bytes + kAtomBytes);
                 const int64_t a = (static_cast<int64_t>(bh) * p.n_t + t) * kAtomBytes;
-                bulk_load(sm.k_sf[st], p.k_sf + a, kAtomBytes, &sm.kv_full[st]);
-                bulk_load(sm.v_sf[st], p.v_sf + a, kAtomBytes, &sm.kv_full[st]);
+                if (is_k) {
+                    tma_load_3d(sm.k[st], &tm_k, &full[st], 0, t * kTile, bh);
+                    bulk_load(sm.k_sf[st], p.k_sf + a, kAtomBytes, &full[st]);
+                } else {
+                    tma_load_3d(sm.v[st], &tm_v, &full[st], t * kTile, 0, bh);
+                    bulk_load(sm.v_sf[st], p.v_sf + a, kAtomBytes, &full[st]);
+                }
                 issued = t + 1;
             }
             if (!ok) raise_abort(sm, p);
             if (sm.abort) {
                 // let the copies still in flight land before the CTA exits
                 int dummy = 0;
-                mbar_wait(&sm.bar_q, 0, p.timeout_ns, &dummy);
+                if (is_k) mbar_wait(&sm.bar_q, 0, p.timeout_ns, &dummy);
                 for (int t = max(0, issued - kStages); t < issued; ++t) {
-                    if ((p.debug_flags & 1) && t == 1) continue;
-                    mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, p.timeout_ns, &dummy);
+                    if (is_k && (p.debug_flags & 1) && t == 1) continue;
+                    mbar_wait(&full[t % kStages], (t / kStages) & 1, p.timeout_ns, &dummy);
                 }
             }
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        warpgroup_reg_dec<kHelperRegs>();
         // ---------------------------------------------------------- MMA
+        // Two issuing threads: warp 9 the score products (into the S
+        // buffers), warp 11 the PV products (into O); a late P therefore never
+        // holds back the next score product.  Descriptors are built once: the
+        // start-address field counts 16-byte units, so + 2 advances an
+        // operand by one 32-byte K step and + 1024 by one 16 KB buffer.
         if (lane == 0) {
-            const uint32_t idesc_qk0 = idesc_mxf8f6f4(128, 128, 0, 0, 0, 0);
-            const uint32_t idesc_pv0 = idesc_mxf8f6f4(128, D, 0, 0, 0, 0);
-            const uint32_t idesc_l0 = idesc_mxf8f6f4(128, 16, 0, 0, 0, 0);
-            const uint32_t qk_swz = D == 128 ? SWZ_128B : SWZ_64B;
-            const uint32_t qk_sbo = D == 128 ? 1024u : 512u;
-            bool ok = mbar_wait(&sm.bar_q, 0, p.timeout_ns, &sm.abort);
-            if (ok) {
-                tc_fence_after();
-                tc_cp_32x128b_x4(tmem + kColSfQ, smem_desc(smem_u32(sm.q_sf), 0, 128, SWZ_NONE));
-                tc_cp_32x128b_x4(tmem + kColSfOnes, smem_desc(smem_u32(sm.ones_sf), 0, 128, SWZ_NONE));
-            }
-            auto issue_pv = [&](int u) {
-                const int pb = u & 1, st = u % kStages;
-                tc_fence_after();
-                tc_cp_32x128b_x4(tmem + kColSfP + 4 * pb, smem_desc(smem_u32(sm.p_sf[pb]), 0, 128, SWZ_NONE));
-                tc_cp_32x128b_x4(tmem + kColSfV + 4 * pb, smem_desc(smem_u32(sm.v_sf[st]), 0, 128, SWZ_NONE));
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t sf = static_cast<uint32_t>(kk);
-                    const uint64_t ad = smem_desc(smem_u32(sm.p[pb]) + 32 * kk, 16, 1024, SWZ_128B);
-                    const uint64_t bd = smem_desc(smem_u32(sm.v[st]) + 32 * kk, 16, 1024, SWZ_128B);
-                    mma_mxf8f6f4(tmem + kColO, ad, bd, idesc_pv0 | (sf << 4) | (sf << 29),
-                                 tmem + kColSfP + 4 * pb, tmem + kColSfV + 4 * pb,
-                                 (u > 0 || kk > 0) ? 1u : 0u);
+            constexpr uint32_t kStageUnits = kTileBytes >> 4, kVUnits = kVBytes >> 4,
+                               kAtomUnits = kAtomBytes >> 4;
+#define FSA_SF(kk) ((static_cast<uint32_t>(kk) << 4) | (static_cast<uint32_t>(kk) << 29))
+            bool ok = true;
+            if (warp == kWarpMma) {
+                const uint32_t qk_swz = D == 128 ? SWZ_128B : SWZ_64B;
+                const uint32_t qk_sbo = D == 128 ? 1024u : 512u;
+                const uint64_t dq = smem_desc(smem_u32(sm.q), 16, qk_sbo, qk_swz);
+                const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, qk_sbo, qk_swz);
+                const uint64_t sfk0 = smem_desc(smem_u32(sm.k_sf[0]), 0, 128, SWZ_NONE);
+                constexpr uint32_t id_qk = idesc_mxf8f6f4(128, 128, 0, 0, 0, 0);
+                ok = mbar_wait(&sm.bar_q, 0, p.timeout_ns, &sm.abort);
+                if (ok) {
+                    tc_fence_after();
+                    tc_cp_32x128b_x4(tmem + kColSfQ, smem_desc(smem_u32(sm.q_sf), 0, 128, SWZ_NONE));
                 }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t sf = static_cast<uint32_t>(kk);
-                    const uint64_t ad = smem_desc(smem_u32(sm.p[pb]) + 32 * kk, 16, 1024, SWZ_128B);
-                    const uint64_t bd = smem_desc(smem_u32(sm.ones) + 32 * kk, 16, 1024, SWZ_128B);
-                    mma_mxf8f6f4(tmem + kColL, ad, bd, idesc_l0 | (sf << 4) | (sf << 29),
-                                 tmem + kColSfP + 4 * pb, tmem + kColSfOnes,
-                                 (u > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(&sm.kv_empty[st]);
-                tc_commit(&sm.p_free[pb]);
-            };
-            // Issue order: a score product as soon as its K tile landed and its
-            // S buffer was released, ahead of any pending PV, so that a softmax
-            // warpgroup never waits behind the other warpgroup's P.  Each
-            // barrier below cannot complete its next phase before this thread
-            // issues the corresponding MMA, so the parities are unambiguous.
-            int qk = 0, pv = 0;
-            uint64_t idle_since = globaltimer_ns();
-            while (ok && pv < p.n_t) {
-                bool progressed = false;
-                if (qk < p.n_t) {
-                    const int st = qk % kStages, sb = qk & 1;
-                    if (mbar_test(&sm.kv_full[st], (qk / kStages) & 1) &&
-                        (qk < 2 || mbar_test(&sm.s_free[sb], ((qk - 2) >> 1) & 1))) {
-                        tc_fence_after();
-                        tc_cp_32x128b_x4(tmem + kColSfK + 4 * sb, smem_desc(smem_u32(sm.k_sf[st]), 0, 128, SWZ_NONE));
-                        for (int kk = 0; kk < nkk; ++kk) {
-                            const uint32_t sf = static_cast<uint32_t>(kk);
-                            const uint64_t ad = smem_desc(smem_u32(sm.q) + 32 * kk, 16, qk_sbo, qk_swz);
-                            const uint64_t bd = smem_desc(smem_u32(sm.k[st]) + 32 * kk, 16, qk_sbo, qk_swz);
-                            mma_mxf8f6f4(tmem + kColS0 + 128 * sb, ad, bd,
-                                         idesc_qk0 | (sf << 4) | (sf << 29), tmem + kColSfQ,
-                                         tmem + kColSfK + 4 * sb, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(&sm.s_full[sb]);
-                        ++qk;
-                        progressed = true;
+                int st = 0;  // K ring stage of tile t
+                for (int t = 0; ok && t < p.n_t; ++t) {
+                    const int sb = t & 1;
+                    // S buffer sb is free once the softmax of tile t - 2 read it
+                    if (t >= 2 && !mbar_wait(&sm.s_free[sb], ((t - 2) >> 1) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
                     }
+                    if (!mbar_wait(&sm.k_full[st], (t / kStages) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfb = tmem + kColSfK + 4 * sb;
+                    tc_cp_32x128b_x4(sfb, sfk0 + kAtomUnits * st);
+                    const uint64_t bk = dk0 + kStageUnits * st;
+                    const uint32_t dst = tmem + kColS0 + 128 * sb;
+                    mma_mxf8f6f4(dst, dq, bk, id_qk | FSA_SF(0), tmem + kColSfQ, sfb, 0u);
+                    mma_mxf8f6f4(dst, dq + 2, bk + 2, id_qk | FSA_SF(1), tmem + kColSfQ, sfb, 1u);
+                    if (nkk == 4) {
+                        mma_mxf8f6f4(dst, dq + 4, bk + 4, id_qk | FSA_SF(2), tmem + kColSfQ, sfb, 1u);
+                        mma_mxf8f6f4(dst, dq + 6, bk + 6, id_qk | FSA_SF(3), tmem + kColSfQ, sfb, 1u);
+                    }
+                    tc_commit(&sm.s_full[sb]);
+                    tc_commit(&sm.k_empty[st]);
+                    st = st + 1 == kStages ? 0 : st + 1;
                 }
-                if (!progressed && pv < qk && mbar_test(&sm.p_full[pv & 1], (pv >> 1) & 1)) {
-                    issue_pv(pv);
-                    ++pv;
-                    progressed = true;
+            } else {
+                const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, SWZ_128B);
+                const uint64_t dp0 = smem_desc(smem_u32(sm.p[0]), 16, 1024, SWZ_128B);
+                const uint64_t sfv0 = smem_desc(smem_u32(sm.v_sf[0]), 0, 128, SWZ_NONE);
+                const uint64_t sfp0 = smem_desc(smem_u32(sm.p_sf[0]), 0, 128, SWZ_NONE);
+                const uint32_t id_pv = idesc_mxf8f6f4(128, D + 16, 0, 0, 0, 0);
+                // unit scales for PV B rows 128-255 (the all-ones rows when D = 128)
+                const uint64_t sf1 = smem_desc(smem_u32(sm.ones_sf), 0, 128, SWZ_NONE);
+                tc_cp_32x128b_x4(tmem + kColSfV + 4, sf1);
+                tc_cp_32x128b_x4(tmem + kColSfV + 12, sf1);
+                int st = 0;  // V ring stage of tile u
+                for (int u = 0; ok && u < p.n_t; ++u) {
+                    const int pb = u & (kPBuf - 1);
+                    if (!mbar_wait(&sm.p_full[pb], (u / kPBuf) & 1, p.timeout_ns, &sm.abort) ||
+                        !mbar_wait(&sm.v_full[st], (u / kStages) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa = tmem + kColSfP + 4 * pb, sfb = tmem + kColSfV + 8 * (u & 1);
+                    tc_cp_32x128b_x4(sfa, sfp0 + kAtomUnits * pb);
+                    tc_cp_32x128b_x4(sfb, sfv0 + kAtomUnits * st);
+                    const uint64_t ap = dp0 + kStageUnits * pb, bv = dv0 + kVUnits * st;
+                    const uint32_t acc = u > 0 ? 1u : 0u;
+                    mma_mxf8f6f4(tmem + kColO, ap, bv, id_pv | FSA_SF(0), sfa, sfb, acc);
+                    mma_mxf8f6f4(tmem + kColO, ap + 2, bv + 2, id_pv | FSA_SF(1), sfa, sfb, 1u);
+                    mma_mxf8f6f4(tmem + kColO, ap + 4, bv + 4, id_pv | FSA_SF(2), sfa, sfb, 1u);
+                    mma_mxf8f6f4(tmem + kColO, ap + 6, bv + 6, id_pv | FSA_SF(3), sfa, sfb, 1u);
+                    tc_commit(&sm.v_empty[st]);
+                    tc_commit(&sm.p_free[pb]);
+                    st = st + 1 == kStages ? 0 : st + 1;
                 }
-                if (progressed) {
-                    idle_since = globaltimer_ns();
-                } else if (sm.abort || globaltimer_ns() - idle_since > p.timeout_ns) {
-                    ok = false;
-                } else {
-                    __nanosleep(32);  // leave the issue slots to the softmax warps
-                }
+                if (ok) tc_commit(&sm.o_full);
             }
-            if (ok) tc_commit(&sm.o_full);
+#undef FSA_SF
             if (!ok) {
                 raise_abort(sm, p);
                 int dummy = 0;
-                tc_commit(&sm.drain);  // wait until every issued MMA/copy retired
-                mbar_wait(&sm.drain, 0, p.timeout_ns, &dummy);
+                uint64_t* drain = warp == kWarpMma ? &sm.drain_qk : &sm.drain_pv;
+                tc_commit(drain);  // wait until every MMA/copy this thread issued retired
+                mbar_wait(drain, 0, p.timeout_ns, &dummy);
             }
         }
     } else {
+        warpgroup_reg_inc<kSoftmaxRegs>();
         // ------------------------------------------------------ softmax
         // Warpgroup wg processes the KV tiles t = wg, wg + 2, ... in TMEM S
         // buffer wg and shared P buffer wg; thread r owns query row r (TMEM
@@ -415,142 +601,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_col = lane_addr + kColS0 + 128 * wg;
         const bool row_valid = (q0 + r) < p.S;
         const int64_t grow = static_cast<int64_t>(bh) * p.S + q0 + r;
-        uint8_t* const prow = sm.p[wg] + (r >> 3) * 1024 + (r & 7) * 128;
-        float m_acc = 0.0f;  // reference maximum in accumulator units
-        unsigned fired_total = 0;
+        RowState rs{0.0f, 0u};
         bool ok = true;
-        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-            const bool w = mbar_wait(bar, parity, p.timeout_ns, &sm.abort);
-            return __all_sync(0xFFFFFFFFu, w);
-        };
-        for (int t = wg, it = 0; t < p.n_t; t += 2, ++it) {
-            if (!wait_all(&sm.s_full[wg], it & 1)) { ok = false; break; }
-            tc_fence_after();
-            const int n_valid = min(kTile, p.S - t * kTile);
-            const bool tail = n_valid < kTile;
-            // pass 1: block maxima and minima of the raw scores
-            float bmax[4], bmin[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(s_col + 64 * h, v0);
-                tmem_ld32(s_col + 64 * h + 32, v1);
-                tmem_ld_wait();
-                if (tail) {
-                    mask32(v0, n_valid - 64 * h);
-                    mask32(v1, n_valid - 64 * h - 32);
-                }
-                maxmin32(v0, bmax[2 * h], bmin[2 * h]);
-                maxmin32(v1, bmax[2 * h + 1], bmin[2 * h + 1]);
-            }
-            const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
-            // frozen reference: tile 0 sets it, the previous tile hands it on
-            if (t > 0) {
-                if (!wait_all(&sm.m_ready[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
-                m_acc = sm.m_ref[wg ^ 1][r];
-            }
-            bool fire = false;
-            float rescale = 1.0f;
-            if (t == 0) {
-                m_acc = tmax;
-            } else if ((tmax - m_acc) * p.sm_scale > p.theta) {
-                fire = true;
-                rescale = expf((m_acc - tmax) * p.sm_scale);
-                m_acc = tmax;
-            }
-            sm.m_ref[wg][r] = m_acc;
-            mbar_arrive(&sm.m_ready[wg]);
-            if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
-            fired_total += (fire && row_valid) ? 1u : 0u;
-            const bool any_fire = __any_sync(0xFFFFFFFFu, fire);
-            if (any_fire) {
-                // recovery: once PV of the previous tile retired, O and l of the
-                // firing rows are scaled by exp(m_old - m_new) in TMEM
-                if (!wait_all(&sm.p_free[wg ^ 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                uint32_t rr[32];
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(lane_addr + kColO + 32 * c, rr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * rescale);
-                    tmem_st32(lane_addr + kColO + 32 * c, rr);
-                }
-                uint32_t lv;
-                tmem_ld1(lane_addr + kColL, lv);
-                tmem_ld_wait();
-                tmem_st1(lane_addr + kColL, __float_as_uint(__uint_as_float(lv) * rescale));
-                tmem_st_wait();
-            }
-            // P buffer wg is free once PV of tile t - 2 retired
-            if (t >= 2 && !wait_all(&sm.p_free[wg], (it - 1) & 1)) { ok = false; break; }
-            const float beta = 16249.0f - p.alpha * m_acc;
-            // pass 2: per 32-key block, E8M0 scale from the block's largest
-            // weight code, then the conversion of its 32 scores
-            uint32_t sfw = 0;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(s_col + 64 * h, v0);
-                tmem_ld32(s_col + 64 * h + 32, v1);
-                tmem_ld_wait();
-                if (h == 1) {
-                    // the whole S tile has been read: release the buffer so the
-                    // next score product can start while this half converts
-                    tc_fence_before();
-                    mbar_arrive(&sm.s_free[wg]);
-                }
-                if (tail) {
-                    mask32(v0, n_valid - 64 * h);
-                    mask32(v1, n_valid - 64 * h - 32);
-                }
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int b = 2 * h + e;
-                    const float bx = h ? (e ? bmax[3] : bmax[2]) : (e ? bmax[1] : bmax[0]);
-                    const float bn = h ? (e ? bmin[3] : bmin[2]) : (e ? bmin[1] : bmin[0]);
-                    const int X = p_scale_exp(code_of(bx, p.alpha, beta), p.p_emax, p.p_mthr) + p.p_off;
-                    const float inv = __int_as_float((127 - X) << 23);
-                    sfw |= static_cast<uint32_t>(X + 127) << (8 * b);
-                    uint32_t w[8];
-                    // E4M3 P: the whole block converts to E4M3 normals when its
-                    // smallest code is a normal bf16 (>= 128) and at least
-                    // 128 X + 15488 (p / 2^X >= 2^-6)
-                    const bool linear = p.p_off == 0 &&
-                        __all_sync(0xFFFFFFFFu, static_cast<int>(code_of(bn, p.alpha, beta)) >= max(128, 128 * X + 15488));
-                    if (linear) {
-                        convert32_linear(e ? v1 : v0, p.alpha, beta,
-                                         static_cast<float>(188728320 - 128 * X), w);
-                    } else if (__any_sync(0xFFFFFFFFu, __fmaf_rn(bn, p.alpha, beta) < 0.0f)) {
-                        convert32<true>(e ? v1 : v0, p.alpha, beta, inv, w);
-                    } else {
-                        convert32<false>(e ? v1 : v0, p.alpha, beta, inv, w);
-                    }
-                    *reinterpret_cast<uint4*>(prow + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4*>(prow + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-                }
-            }
-            tc_fence_before();
-            *reinterpret_cast<uint32_t*>(sm.p_sf[wg] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
-            fence_async_smem();
-            mbar_arrive(&sm.p_full[wg]);
+        const int t_tail = (p.S % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
+        for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it) {
+            ok = (t == t_tail)
+                     ? softmax_tile<kE4M3, true>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, rs)
+                     : softmax_tile<kE4M3, false>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, rs);
         }
         if (!ok) raise_abort(sm, p);
         if (ok) {
-            ok = wait_all(&sm.o_full, 0);
+            ok = wait_warp(&sm.o_full, 0, p, sm);
             if (!ok) raise_abort(sm, p);
         }
         if (ok) {
             // epilogue: warpgroup wg writes columns [wg * D/2, (wg+1) * D/2)
             tc_fence_after();
             uint32_t lv;
-            tmem_ld1(lane_addr + kColL, lv);
+            tmem_ld1(lane_addr + kColO + D, lv);
             tmem_ld_wait();
             const float l = __uint_as_float(lv);
             for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
                 uint32_t rr[32];
                 tmem_ld32(lane_addr + kColO + 32 * c, rr);
                 tmem_ld_wait();
+                tmem_reg_dep(rr);
                 if (row_valid) {
                     uint32_t packed[16];
 #pragma unroll
@@ -566,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (p.rollback_count) {
-                unsigned tot = fired_total;
+                unsigned tot = rs.fired;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
                 if (lane == 0 && tot) atomicAdd(p.rollback_count, static_cast<unsigned long long>(tot));
@@ -600,19 +675,22 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.sm_scale = a.sm_scale;
     p.alpha = static_cast<float>(128.0 * 1.4426950408889634 * static_cast<double>(a.sm_scale));
     p.theta = a.threshold;
-    const bool p_e4m3 = (a.fmt == 0);
-    p.p_off = p_e4m3 ? 0 : 6;
-    p.p_emax = p_e4m3 ? 8 : 2;
-    p.p_mthr = p_e4m3 ? 0x60u : 0x70u;
     p.timeout_ns = a.timeout_ns;
     p.debug_flags = a.debug_flags;
     const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(fsa_attn_fwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4
+    auto kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<true> : fsa_attn_fwd_kernel<false>;
+    // the in-kernel register split assumes exactly kLaunchRegs per thread at
+    // launch; anything else could make the increase wait forever
+    cudaFuncAttributes fa{};
+    cudaError_t ea = cudaFuncGetAttributes(&fa, kernel);
+    if (ea != cudaSuccess) return ea;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(p.n_t), static_cast<unsigned>(a.BH));
-    fsa_attn_fwd_kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
     return cudaGetLastError();
 }
 

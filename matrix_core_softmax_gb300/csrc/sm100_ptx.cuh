@@ -228,11 +228,44 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r)
                  : "memory");
 }
+// Waits for this thread's outstanding TMEM loads and marks the 32 destination
+// registers as produced by the wait, so no use of them can be scheduled
+// before it.
+#define FSA_D8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                  "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : FSA_D8(0), FSA_D8(8), FSA_D8(16), FSA_D8(24)
+                 :
+                 : "memory");
+}
+#undef FSA_D8
+// Marks 32 registers as redefined here (emits no instruction): placed after a
+// tcgen05.wait::ld, it keeps every use of a TMEM load's destination registers
+// after the wait.
+#define FSA_D8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                  "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_reg_dep(uint32_t (&r)[32]) {
+    asm volatile("" : FSA_D8(0), FSA_D8(8), FSA_D8(16), FSA_D8(24) : : "memory");
+}
+#undef FSA_D8
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Per-warpgroup register reconfiguration (all 128 threads of the warpgroup
+// execute it).  The sum over warpgroups must not exceed the block's launch
+// allocation, or an increase waits forever.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ------------------------------------------------------- conversions --
