@@ -77,7 +77,7 @@ struct __align__(1024) Smem {
     uint8_t v_sf[kStages][kAtomBytes];
     uint8_t p_sf[kPBuf][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
-    float m_ref[2][128];  // reference maximum handed from one warpgroup to the other
+    float tmax_x[8][128];  // row maxima of tile t in slot t % 8, read by the other warpgroup
     uint64_t bar_q;
     uint64_t k_full[kStages];   // K tile landed
     uint64_t k_empty[kStages];  // score product that read the K tile retired
@@ -87,7 +87,7 @@ struct __align__(1024) Smem {
     uint64_t s_free[2];
     uint64_t p_full[kPBuf];
     uint64_t p_free[kPBuf];  // PV of the tile that used P buffer i retired
-    uint64_t m_ready[2]; // warpgroup i published the reference after its tile
+    uint64_t m_ready[8]; // slot i of tmax_x written (tiles i, i + 8, ...)
     uint64_t o_full;
     uint64_t drain_qk, drain_pv;
     uint32_t tmem_base;
@@ -237,41 +237,90 @@ template <bool kE4M3> struct PType;
 template <> struct PType<true> { static constexpr int kOff = 0, kEmax = 8; static constexpr uint32_t kMthr = 0x60; };
 template <> struct PType<false> { static constexpr int kOff = 6, kEmax = 2; static constexpr uint32_t kMthr = 0x70; };
 
-// Pass 2 for one 32-key block b of row r: the block's E8M0 scale from its
-// largest weight code, the conversion of its 32 scores, and the two 16-byte
-// stores into the 128-byte-swizzled P row.  Returns the scale byte.
+// Pass 2 for one 32-key block b of row r: the block's E8M0 scale exponent
+// from its largest weight code (returned), the conversion of its 32 scores
+// and the two 16-byte stores into the 128-byte-swizzled P row.
 template <bool kE4M3>
-__device__ __forceinline__ uint32_t convert_block(const uint32_t (&v)[32], int b, float bx, float bn,
-                                                  float alpha, float beta, uint8_t* prow, int r) {
+__device__ __forceinline__ int block_scale_exp(float bx, float alpha, float beta) {
     using T = PType<kE4M3>;
-    const int X = p_scale_exp(code_of(bx, alpha, beta), T::kEmax, T::kMthr) + T::kOff;
-    const float inv = __int_as_float((127 - X) << 23);
-    uint32_t w[8];
-    if (kE4M3) {
-        // the whole block converts to E4M3 normals when its smallest code is a
-        // normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6)
-        if (__all_sync(0xFFFFFFFFu,
-                       static_cast<int>(code_of(bn, alpha, beta)) >= max(128, 128 * X + 15488))) {
-            // kx = 188728320 - 128 X; one unit of X is 8 units in the last
-            // place of a float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f
-            convert32_linear(v, alpha, beta, __int_as_float(0x4D33FC40 - 8 * X), w);
-        } else {
-            convert32<true>(v, alpha, beta, inv, w);
-        }
-    } else {
-        if (__any_sync(0xFFFFFFFFu, __fmaf_rn(bn, alpha, beta) < 0.0f))
-            convert32<true>(v, alpha, beta, inv, w);
-        else
-            convert32<false>(v, alpha, beta, inv, w);
-    }
+    return p_scale_exp(code_of(bx, alpha, beta), T::kEmax, T::kMthr) + T::kOff;
+}
+
+__device__ __forceinline__ void store_p_block(uint8_t* prow, int r, int b, const uint32_t (&w)[8]) {
     *reinterpret_cast<uint4*>(prow + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(prow + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-    return static_cast<uint32_t>(X + 127);
+}
+
+// E4M3 P: the whole block converts to E4M3 normals when its smallest code is
+// a normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6).
+__device__ __forceinline__ bool block_is_linear(float bn, int X, float alpha, float beta) {
+    return static_cast<int>(code_of(bn, alpha, beta)) >= max(128, 128 * X + 15488);
+}
+
+// The general conversion of one block (subnormal P elements, clamped codes).
+template <bool kE4M3>
+__device__ __forceinline__ void convert_block_general(const uint32_t (&v)[32], int b, float bn, int X,
+                                                      float alpha, float beta, uint8_t* prow, int r) {
+    const float inv = __int_as_float((127 - X) << 23);
+    uint32_t w[8];
+    if (kE4M3 || __any_sync(0xFFFFFFFFu, __fmaf_rn(bn, alpha, beta) < 0.0f))
+        convert32<true>(v, alpha, beta, inv, w);
+    else
+        convert32<false>(v, alpha, beta, inv, w);
+    store_p_block(prow, r, b, w);
+}
+
+// kx = 188728320 - 128 X: one unit of X is 8 units in the last place of a
+// float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f.
+__device__ __forceinline__ float linear_kx(int X) { return __int_as_float(0x4D33FC40 - 8 * X); }
+
+// One arrival per warp: the lanes' preceding shared-memory writes and TMEM
+// reads are ordered before lane 0's release-arrive by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Params& p, Smem& sm) {
     const bool w = mbar_wait(bar, parity, p.timeout_ns, &sm.abort);
     return __all_sync(0xFFFFFFFFu, w);
+}
+
+// The two-stage conversion of a whole tile for row r (four 32-key blocks):
+// block scales from the block maxima, then E4M3 patterns into the P row.
+// Returns the four E8M0 scale bytes packed into a word.
+template <bool kE4M3>
+__device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
+                                                 const uint32_t (&s2)[32], const uint32_t (&s3)[32],
+                                                 const float (&bmax)[4], const float (&bmin)[4],
+                                                 float alpha, float beta, uint8_t* prow, int r) {
+    const int X0 = block_scale_exp<kE4M3>(bmax[0], alpha, beta);
+    const int X1 = block_scale_exp<kE4M3>(bmax[1], alpha, beta);
+    const int X2 = block_scale_exp<kE4M3>(bmax[2], alpha, beta);
+    const int X3 = block_scale_exp<kE4M3>(bmax[3], alpha, beta);
+    // one decision for the whole tile: every block of every row of the warp
+    // converts linearly (the common case for MXFP8), else block by block
+    if (kE4M3 && __all_sync(0xFFFFFFFFu, block_is_linear(bmin[0], X0, alpha, beta) &&
+                                             block_is_linear(bmin[1], X1, alpha, beta) &&
+                                             block_is_linear(bmin[2], X2, alpha, beta) &&
+                                             block_is_linear(bmin[3], X3, alpha, beta))) {
+        uint32_t w0[8], w1[8], w2[8], w3[8];
+        convert32_linear(s0, alpha, beta, linear_kx(X0), w0);
+        convert32_linear(s1, alpha, beta, linear_kx(X1), w1);
+        convert32_linear(s2, alpha, beta, linear_kx(X2), w2);
+        convert32_linear(s3, alpha, beta, linear_kx(X3), w3);
+        store_p_block(prow, r, 0, w0);
+        store_p_block(prow, r, 1, w1);
+        store_p_block(prow, r, 2, w2);
+        store_p_block(prow, r, 3, w3);
+    } else {
+        convert_block_general<kE4M3>(s0, 0, bmin[0], X0, alpha, beta, prow, r);
+        convert_block_general<kE4M3>(s1, 1, bmin[1], X1, alpha, beta, prow, r);
+        convert_block_general<kE4M3>(s2, 2, bmin[2], X2, alpha, beta, prow, r);
+        convert_block_general<kE4M3>(s3, 3, bmin[3], X3, alpha, beta, prow, r);
+    }
+    return static_cast<uint32_t>(X0 + 127) | (static_cast<uint32_t>(X1 + 127) << 8) |
+           (static_cast<uint32_t>(X2 + 127) << 16) | (static_cast<uint32_t>(X3 + 127) << 24);
 }
 
 // Per-row state of a softmax thread.
@@ -305,7 +354,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tmem_reg_dep(s3);
     // the whole tile is in registers: the next score product may reuse S
     tc_fence_before();
-    mbar_arrive(&sm.s_free[wg]);
+    warp_arrive(&sm.s_free[wg]);
     if (kTail) {
         // keys >= S are masked before the gate and the conversion
         const int n_valid = p.S - t * kTile;
@@ -320,10 +369,18 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     maxmin32(s2, bmax[2], bmin[2]);
     maxmin32(s3, bmax[3], bmin[3]);
     const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
-    // frozen reference: tile 0 sets it, the previous tile hands it on
+    // publish this tile's row maximum for the other warpgroup in slot t % 8;
+    // the reader consumes it during its tile t + 1, long before this
+    // warpgroup rewrites the slot at tile t + 8 (which needs the reader's
+    // tile t + 7 maximum)
+    sm.tmax_x[t & 7][r] = tmax;
+    warp_arrive(&sm.m_ready[t & 7]);
+    // frozen reference: replay the gate over the previous tile's maximum,
+    // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
     if (t > 0) {
-        if (!wait_warp(&sm.m_ready[wg ^ 1], ((t - 1) >> 1) & 1, p, sm)) return false;
-        rs.m_acc = sm.m_ref[wg ^ 1][r];
+        if (!wait_warp(&sm.m_ready[(t - 1) & 7], ((t - 1) >> 3) & 1, p, sm)) return false;
+        const float prev = sm.tmax_x[(t - 1) & 7][r];
+        if (t == 1 || (prev - rs.m_acc) * p.sm_scale > p.theta) rs.m_acc = prev;
     }
     bool fire = false;
     float rescale = 1.0f;
@@ -334,8 +391,6 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         rescale = expf((rs.m_acc - tmax) * p.sm_scale);
         rs.m_acc = tmax;
     }
-    sm.m_ref[wg][r] = rs.m_acc;
-    mbar_arrive(&sm.m_ready[wg]);
     if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
     rs.fired += (fire && row_valid) ? 1u : 0u;
     // P buffer pb is free once PV of tile t - 4 retired.  Waited first: PV
@@ -363,15 +418,12 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
         tmem_st_wait();
     }
-    const float beta = 16249.0f - p.alpha * rs.m_acc;
-    uint32_t sfw = convert_block<kE4M3>(s0, 0, bmax[0], bmin[0], p.alpha, beta, prow, r);
-    sfw |= convert_block<kE4M3>(s1, 1, bmax[1], bmin[1], p.alpha, beta, prow, r) << 8;
-    sfw |= convert_block<kE4M3>(s2, 2, bmax[2], bmin[2], p.alpha, beta, prow, r) << 16;
-    sfw |= convert_block<kE4M3>(s3, 3, bmax[3], bmin[3], p.alpha, beta, prow, r) << 24;
+    const uint32_t sfw =
+        convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc, prow, r);
     tc_fence_before();
     *reinterpret_cast<uint32_t*>(sm.p_sf[pb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
     fence_async_smem();
-    mbar_arrive(&sm.p_full[pb]);
+    warp_arrive(&sm.p_full[pb]);
     return true;
 }
 
@@ -413,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_free[i], 128);
-            mbar_init(&sm.m_ready[i], 128);
+            mbar_init(&sm.s_free[i], 4);  // one arrival per softmax warp
         }
+        for (int i = 0; i < 8; ++i) mbar_init(&sm.m_ready[i], 4);
         for (int i = 0; i < kPBuf; ++i) {
-            mbar_init(&sm.p_full[i], 128);
+            mbar_init(&sm.p_full[i], 4);
             mbar_init(&sm.p_free[i], 1);
         }
         mbar_init(&sm.o_full, 1);
@@ -593,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ softmax
         // Warpgroup wg processes the KV tiles t = wg, wg + 2, ... in TMEM S
         // buffer wg and shared P buffer wg; thread r owns query row r (TMEM
-        // lane r).  The reference maximum travels between the warpgroups
-        // through m_ref / m_ready after every tile.
+        // lane r).  Tile maxima travel between the warpgroups through
+        // tmax_x / m_ready; each warpgroup replays the gate over them.
         const int wg = warp >> 2;
         const int r = tid & 127;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
