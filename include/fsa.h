@@ -180,6 +180,33 @@ FSA_API uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fm
 FSA_API fsa_status fsa_bf16_attention_fwd(const void *q, const void *k, const void *v, void *o,
                                   int B, int H, int S, int D, void *stream);
 
+/*
+ * fsa_attention_fwd_noalloc -- fsa_attention_fwd without any device memory
+ * allocation.  (An addition of this library; the pages have no counterpart.)
+ *
+ * For callers that must not allocate or free device memory once they are
+ * running -- for example code whose device memory budget is owned entirely by
+ * its own allocator, or a latency-critical loop that cannot afford
+ * cudaMalloc/cudaFree (which may synchronise the device or fail under memory
+ * pressure).  Instead of the cached workspace, the MX copies of q, k, v live in
+ * a fixed 64 MiB array compiled into the library: every device that loads the
+ * library holds it until the process exits.
+ *  - Same arguments, layouts and results as fsa_attention_fwd.
+ *  - Shapes whose workspace (fsa_attention_workspace_size) exceeds 64 MiB --
+ *    roughly B*H*S*D above 21 million -- return FSA_ERR_INVALID_ARGUMENT.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (and clears a status word); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents: calls that overlap on the GPU (different streams, or several
+ *    host threads) race on it and must be serialised by the caller.
+ *  - A kernel whose bounded wait ran out records that in a status word of
+ *    this entry point, not in the word fsa_get_device_error reads.
+ */
+FSA_API fsa_status fsa_attention_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
+                                             int B, int H, int S, int D, int fmt,
+                                             float threshold, void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: FSA_OK, FSA_ERR_TIMEOUT, or FSA_ERR_CUDA if the sync
  * itself failed. */

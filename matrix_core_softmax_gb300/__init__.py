@@ -27,7 +27,7 @@ STATUS = {0: "FSA_OK", 1: "FSA_ERR_INVALID_ARGUMENT", 2: "FSA_ERR_UNSUPPORTED",
 # every symbol include/fsa.h declares
 EXPORTS = ("fsa_quantize_mx", "fsa_attention_fwd", "fsa_attention_fwd_ex",
            "fsa_attention_prepare", "fsa_attention_run", "fsa_attention_workspace_size", "fsa_bf16_attention_fwd", "fsa_get_device_error",
-           "fsa_status_string", "fsa_release_workspace")
+           "fsa_status_string", "fsa_release_workspace", "fsa_attention_fwd_noalloc")
 
 
 class FsaError(RuntimeError):
@@ -76,6 +76,8 @@ def load(path: str | None = None):
             lib.fsa_attention_run.restype = I
             lib.fsa_attention_workspace_size.argtypes = [I, I, I, I, I]
             lib.fsa_attention_workspace_size.restype = ctypes.c_uint64
+            lib.fsa_attention_fwd_noalloc.argtypes = [V, V, V, V, I, I, I, I, I, F, V]
+            lib.fsa_attention_fwd_noalloc.restype = I
             lib.fsa_bf16_attention_fwd.argtypes = [V, V, V, V, I, I, I, I, V]
             lib.fsa_bf16_attention_fwd.restype = I
             lib.fsa_get_device_error.argtypes = [V]
@@ -188,6 +190,20 @@ def attention_run(workspace, out, fmt: str = "mxfp8", threshold: float = 8.0, *,
                                     FORMATS[fmt], float(threshold), ctypes.byref(opt),
                                     _stream(stream)), "fsa_attention_run")
     return out
+
+
+def attention_fwd_noalloc(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
+                          stream=None):
+    """fsa_attention_fwd_noalloc: the fused attention with the library's fixed
+    64 MiB scratch array instead of an allocated workspace (see include/fsa.h)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bhsd(t, n)
+    B, H, S, D = q.shape
+    o = torch.empty_like(q) if out is None else out
+    _check(load().fsa_attention_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
+                                            FORMATS[fmt], float(threshold), _stream(stream)),
+           "fsa_attention_fwd_noalloc")
+    return o
 
 
 def bf16_attention_fwd(q, k, v, *, out=None, stream=None):

@@ -412,3 +412,79 @@ void fsa_release_workspace(void) {
 }
 
 }  // extern "C"
+
+// --------------------------------------------------------------------------
+// fsa_attention_fwd_noalloc: the fused attention with its scratch in a
+// fixed-size device array that belongs to the library image, for callers
+// that must not allocate or free device memory once running.
+namespace fsa {
+namespace {
+
+constexpr size_t kNoAllocBytes = size_t(64) << 20;  // 64 MiB per device, held until exit
+static __device__ __align__(256) uint8_t g_noalloc_ws[kNoAllocBytes];
+static __device__ __align__(256) unsigned int g_noalloc_status;  // kernels' bounded-wait status
+
+struct NoAllocDevice {
+    void* ws = nullptr;
+    unsigned int* status = nullptr;
+    int arch_ok = -1;
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// Device addresses of the two arrays on the current device (looked up once
+// per device, with that device current); no allocation.
+fsa_status noalloc_setup(int dev, NoAllocDevice** out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc[dev];
+    if (d.arch_ok < 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        d.arch_ok = (major == 10 && (minor == 0 || minor == 3)) ? 1 : 0;
+    }
+    if (!d.arch_ok) return FSA_ERR_UNSUPPORTED;
+    if (!d.ws) {
+        void* ws = nullptr;
+        void* st = nullptr;
+        if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess ||
+            cudaGetSymbolAddress(&st, g_noalloc_status) != cudaSuccess) {
+            cudaGetLastError();
+            return FSA_ERR_CUDA;
+        }
+        // the status word must start at zero; nothing else needs clearing
+        // (every call rewrites the codes and resets the scale atoms)
+        if (cudaMemset(st, 0, sizeof(unsigned int)) != cudaSuccess) return FSA_ERR_CUDA;
+        d.ws = ws;
+        d.status = static_cast<unsigned int*>(st);
+    }
+    *out = &d;
+    return FSA_OK;
+}
+
+}  // namespace
+}  // namespace fsa
+
+extern "C" fsa_status fsa_attention_fwd_noalloc(const void* q, const void* k, const void* v,
+                                                void* o, int B, int H, int S, int D, int fmt,
+                                                float threshold, void* stream) {
+    using namespace fsa;
+    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    if (s != FSA_OK) return s;
+    fsa_options defaults{};
+    s = check_run_args(fmt, threshold, defaults);
+    if (s != FSA_OK) return s;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (attn_workspace_bytes(BH, S, D) > kNoAllocBytes) return FSA_ERR_INVALID_ARGUMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FSA_ERR_UNSUPPORTED;
+    NoAllocDevice* d = nullptr;
+    s = noalloc_setup(dev, &d);
+    if (s != FSA_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = prepare_impl(q, k, v, BH, S, D, fmt, d->ws, st);
+    if (s != FSA_OK) return s;
+    return run_impl(d->ws, o, BH, S, D, fmt, threshold, defaults, d->status, st);
+}
