@@ -110,28 +110,15 @@ struct Params {
     float theta;     // gate threshold, natural-log score units
     uint64_t timeout_ns;
     int debug_flags;
+    // 2^8 and 2^16, held in registers: byte and half-word packing as an
+    // integer multiply-add runs on the FMA pipe, while a constant multiplier
+    // would become a shift on the integer ALU, the softmax warps' busiest pipe
+    uint32_t mul8, mul16;
 };
 
 __device__ __forceinline__ void raise_abort(Smem& sm, const Params& p) {
     sm.abort = 1;
     atomicOr(p.err_word, kErrTimeout);
-}
-
-// Smallest X with amax <= max_elem * 2^X, from the bf16 pattern of amax.
-__device__ __forceinline__ int p_scale_exp(uint32_t amax_bf16, int emax, uint32_t mthr) {
-    if (amax_bf16 == 0) return -127;
-    int E = static_cast<int>(amax_bf16 >> 7);
-    uint32_t m = amax_bf16 & 0x7Fu;
-    int e;
-    if (E == 0) {
-        int nb = 32 - __clz(m);
-        e = nb - 134;
-        m = (m << (8 - nb)) & 0x7Fu;
-    } else {
-        e = E - 127;
-    }
-    int X = e - emax + (m > mthr ? 1 : 0);
-    return min(127, max(-127, X));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -169,22 +156,19 @@ __device__ __forceinline__ void mask32(uint32_t (&v)[32], int n_valid) {
         if (j >= n_valid) v[j] = 0xFF800000u;
 }
 
-// Schraudolph code of a single score: rne(max(alpha * s + beta, 0)).  The
-// upper clamp at 0x7F7F is never active: a row's scores never pass its
-// reference by more than theta <= 80, so y <= 128 * (127 + 80 log2 e) - 7.
-__device__ __forceinline__ uint32_t code_of(float s, float alpha, float beta) {
-    const float y = fmaxf(__fmaf_rn(s, alpha, beta), 0.0f);
-    return __float_as_uint(__fadd_rn(y, kMagic)) & 0xFFFFu;
-}
+constexpr int kMagicBits = 0x4B400000;  // bit pattern of kMagic
 
 // Two-stage conversion of 32 scores of one 32-key block: bf16 weight code
 // (integer reinterpretation) -> E4M3 pattern of p * inv, inv = 2^-(X+off).
-// Writes 8 words, element i in byte i % 4 of word i / 4.
+// Writes 8 words, element i in byte i % 4 of word i / 4.  The low 16 bits
+// of y + kMagic are the code, so (y + kMagic) * 2^16 (mod 2^32) is the bf16
+// weight as an FP32 pattern.
 template <bool kClamp>
 __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, float beta,
-                                          float inv, uint32_t (&w)[8]) {
+                                          float inv, uint32_t mul16, uint32_t (&w)[8]) {
     const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
     const float2 m2 = make_float2(kMagic, kMagic), i2 = make_float2(inv, inv);
+    uint32_t e[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         float2 y = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
@@ -194,15 +178,13 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, 
             y.y = fmaxf(y.y, 0.0f);
         }
         y = __fadd2_rn(y, m2);
-        const float2 pw = make_float2(__uint_as_float(__float_as_uint(y.x) << 16),
-                                      __uint_as_float(__float_as_uint(y.y) << 16));
+        const float2 pw = make_float2(__uint_as_float(__float_as_uint(y.x) * mul16),
+                                      __uint_as_float(__float_as_uint(y.y) * mul16));
         const float2 q = __fmul2_rn(pw, i2);
-        const uint32_t e = cvt_e4m3x2(q.x, q.y);
-        if (i & 1)
-            w[i >> 1] |= e << 16;
-        else
-            w[i >> 1] = e;
+        e[i] = cvt_e4m3x2(q.x, q.y);
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = e[2 * i + 1] * mul16 + e[2 * i];
 }
 
 // E4M3 P when every score of the 32-key block converts to an E4M3 normal
@@ -213,9 +195,11 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, 
 // perform both roundings: + 1.5 * 2^23 rounds y to the integer code, then
 // + kx (= 1.5 * 2^27 - 1.5 * 2^23 - 15360 - 128 X, a multiple of 16) lands
 // in [2^27, 2^28) where one unit in the last place is 16, rounding the
-// quotient to nearest even; its low byte is the E4M3 code.
+// quotient to nearest even; its pattern is 0x4D400000 + the E4M3 code.
+// Packing: the pattern's low 16 bits are the code alone, so
+// pattern_1 * 2^8 + pattern_0 holds codes 0 and 1 in its low half-word.
 __device__ __forceinline__ void convert32_linear(const uint32_t (&v)[32], float alpha, float beta,
-                                                 float kx, uint32_t (&w)[8]) {
+                                                 float kx, uint32_t mul8, uint32_t (&w)[8]) {
     const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
     const float2 m2 = make_float2(kMagic, kMagic), k2 = make_float2(kx, kx);
 #pragma unroll
@@ -224,8 +208,8 @@ __device__ __forceinline__ void convert32_linear(const uint32_t (&v)[32], float 
         float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), a2, b2);
         y0 = __fadd2_rn(__fadd2_rn(y0, m2), k2);
         y1 = __fadd2_rn(__fadd2_rn(y1, m2), k2);
-        const uint32_t lo = __byte_perm(__float_as_uint(y0.x), __float_as_uint(y0.y), 0x0040);
-        const uint32_t hi = __byte_perm(__float_as_uint(y1.x), __float_as_uint(y1.y), 0x0040);
+        const uint32_t lo = __float_as_uint(y0.y) * mul8 + __float_as_uint(y0.x);
+        const uint32_t hi = __float_as_uint(y1.y) * mul8 + __float_as_uint(y1.x);
         w[i] = __byte_perm(lo, hi, 0x5410);
     }
 }
@@ -237,13 +221,20 @@ template <bool kE4M3> struct PType;
 template <> struct PType<true> { static constexpr int kOff = 0, kEmax = 8; static constexpr uint32_t kMthr = 0x60; };
 template <> struct PType<false> { static constexpr int kOff = 6, kEmax = 2; static constexpr uint32_t kMthr = 0x70; };
 
-// Pass 2 for one 32-key block b of row r: the block's E8M0 scale exponent
-// from its largest weight code (returned), the conversion of its 32 scores
-// and the two 16-byte stores into the 128-byte-swizzled P row.
+// E8M0 scale byte (X + 127, X including the E2M3 offset) of one 32-key
+// block from its largest score.  With y = alpha * bmax + beta, y + kMagic
+// holds the block's largest weight code c in its low bits (c <= 0 when the
+// weight clamps to zero); the rule "smallest X with p_max <= max_elem * 2^X"
+// on the bf16 pattern c (exponent field E, mantissa m) gives
+// X + 127 = E - emax + (m > mthr) = floor((c + 127 - mthr) / 128) - emax,
+// clamped at X = -127, which also covers every bf16 subnormal code.  y is
+// clamped at -1 first so that c stays in range for any score.
 template <bool kE4M3>
-__device__ __forceinline__ int block_scale_exp(float bx, float alpha, float beta) {
+__device__ __forceinline__ int block_scale_byte(float bmax, float alpha, float beta) {
     using T = PType<kE4M3>;
-    return p_scale_exp(code_of(bx, alpha, beta), T::kEmax, T::kMthr) + T::kOff;
+    const float y = fmaxf(__fmaf_rn(bmax, alpha, beta), -1.0f);
+    const int c = static_cast<int>(__float_as_uint(__fadd_rn(y, kMagic))) - kMagicBits;
+    return max((c + 127 - static_cast<int>(T::kMthr) - 128 * T::kEmax) >> 7, 0) + T::kOff;
 }
 
 __device__ __forceinline__ void store_p_block(uint8_t* prow, int r, int b, const uint32_t (&w)[8]) {
@@ -252,27 +243,28 @@ __device__ __forceinline__ void store_p_block(uint8_t* prow, int r, int b, const
 }
 
 // E4M3 P: the whole block converts to E4M3 normals when its smallest code is
-// a normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6).
-__device__ __forceinline__ bool block_is_linear(float bn, int X, float alpha, float beta) {
-    return static_cast<int>(code_of(bn, alpha, beta)) >= max(128, 128 * X + 15488);
+// a normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6), with
+// X = sb - 127.  Compared on the FP32 patterns of y + kMagic (signed, so a
+// negative y fails).
+__device__ __forceinline__ bool block_is_linear(float bn, int sb, float alpha, float beta) {
+    const int cmin = static_cast<int>(__float_as_uint(__fadd_rn(__fmaf_rn(bn, alpha, beta), kMagic)));
+    return cmin >= kMagicBits + 128 * max(sb - 6, 1);
 }
 
-// The general conversion of one block (subnormal P elements, clamped codes).
-template <bool kE4M3>
-__device__ __forceinline__ void convert_block_general(const uint32_t (&v)[32], int b, float bn, int X,
-                                                      float alpha, float beta, uint8_t* prow, int r) {
-    const float inv = __int_as_float((127 - X) << 23);
+// The general conversion of one block (subnormal P elements, clamped codes);
+// inv = 2^-X with X = sb - 127.
+template <bool kClamp>
+__device__ __forceinline__ void convert_block_general(const uint32_t (&v)[32], int b, int sb, float alpha,
+                                                      float beta, uint32_t mul16, uint8_t* prow, int r) {
     uint32_t w[8];
-    if (kE4M3 || __any_sync(0xFFFFFFFFu, __fmaf_rn(bn, alpha, beta) < 0.0f))
-        convert32<true>(v, alpha, beta, inv, w);
-    else
-        convert32<false>(v, alpha, beta, inv, w);
+    convert32<kClamp>(v, alpha, beta, __int_as_float((254 - sb) << 23), mul16, w);
     store_p_block(prow, r, b, w);
 }
 
 // kx = 188728320 - 128 X: one unit of X is 8 units in the last place of a
-// float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f.
-__device__ __forceinline__ float linear_kx(int X) { return __int_as_float(0x4D33FC40 - 8 * X); }
+// float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f; with X = sb - 127
+// the pattern is 0x4D340038 - 8 sb.
+__device__ __forceinline__ float linear_kx(int sb) { return __int_as_float(0x4D340038 - 8 * sb); }
 
 // One arrival per warp: the lanes' preceding shared-memory writes and TMEM
 // reads are ordered before lane 0's release-arrive by the warp barrier.
@@ -293,34 +285,44 @@ template <bool kE4M3>
 __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
                                                  const uint32_t (&s2)[32], const uint32_t (&s3)[32],
                                                  const float (&bmax)[4], const float (&bmin)[4],
-                                                 float alpha, float beta, uint8_t* prow, int r) {
-    const int X0 = block_scale_exp<kE4M3>(bmax[0], alpha, beta);
-    const int X1 = block_scale_exp<kE4M3>(bmax[1], alpha, beta);
-    const int X2 = block_scale_exp<kE4M3>(bmax[2], alpha, beta);
-    const int X3 = block_scale_exp<kE4M3>(bmax[3], alpha, beta);
+                                                 float alpha, float beta, uint32_t mul8, uint32_t mul16,
+                                                 uint8_t* prow, int r) {
+    const int sb0 = block_scale_byte<kE4M3>(bmax[0], alpha, beta);
+    const int sb1 = block_scale_byte<kE4M3>(bmax[1], alpha, beta);
+    const int sb2 = block_scale_byte<kE4M3>(bmax[2], alpha, beta);
+    const int sb3 = block_scale_byte<kE4M3>(bmax[3], alpha, beta);
     // one decision for the whole tile: every block of every row of the warp
     // converts linearly (the common case for MXFP8), else block by block
-    if (kE4M3 && __all_sync(0xFFFFFFFFu, block_is_linear(bmin[0], X0, alpha, beta) &&
-                                             block_is_linear(bmin[1], X1, alpha, beta) &&
-                                             block_is_linear(bmin[2], X2, alpha, beta) &&
-                                             block_is_linear(bmin[3], X3, alpha, beta))) {
+    if (kE4M3 && __all_sync(0xFFFFFFFFu, block_is_linear(bmin[0], sb0, alpha, beta) &&
+                                             block_is_linear(bmin[1], sb1, alpha, beta) &&
+                                             block_is_linear(bmin[2], sb2, alpha, beta) &&
+                                             block_is_linear(bmin[3], sb3, alpha, beta))) {
         uint32_t w0[8], w1[8], w2[8], w3[8];
-        convert32_linear(s0, alpha, beta, linear_kx(X0), w0);
-        convert32_linear(s1, alpha, beta, linear_kx(X1), w1);
-        convert32_linear(s2, alpha, beta, linear_kx(X2), w2);
-        convert32_linear(s3, alpha, beta, linear_kx(X3), w3);
+        convert32_linear(s0, alpha, beta, linear_kx(sb0), mul8, w0);
+        convert32_linear(s1, alpha, beta, linear_kx(sb1), mul8, w1);
+        convert32_linear(s2, alpha, beta, linear_kx(sb2), mul8, w2);
+        convert32_linear(s3, alpha, beta, linear_kx(sb3), mul8, w3);
         store_p_block(prow, r, 0, w0);
         store_p_block(prow, r, 1, w1);
         store_p_block(prow, r, 2, w2);
         store_p_block(prow, r, 3, w3);
+    } else if (kE4M3 || __any_sync(0xFFFFFFFFu,
+                                   __fmaf_rn(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                             alpha, beta) < 0.0f)) {
+        // some weight of the warp's rows clamps to zero
+        convert_block_general<true>(s0, 0, sb0, alpha, beta, mul16, prow, r);
+        convert_block_general<true>(s1, 1, sb1, alpha, beta, mul16, prow, r);
+        convert_block_general<true>(s2, 2, sb2, alpha, beta, mul16, prow, r);
+        convert_block_general<true>(s3, 3, sb3, alpha, beta, mul16, prow, r);
     } else {
-        convert_block_general<kE4M3>(s0, 0, bmin[0], X0, alpha, beta, prow, r);
-        convert_block_general<kE4M3>(s1, 1, bmin[1], X1, alpha, beta, prow, r);
-        convert_block_general<kE4M3>(s2, 2, bmin[2], X2, alpha, beta, prow, r);
-        convert_block_general<kE4M3>(s3, 3, bmin[3], X3, alpha, beta, prow, r);
+        convert_block_general<false>(s0, 0, sb0, alpha, beta, mul16, prow, r);
+        convert_block_general<false>(s1, 1, sb1, alpha, beta, mul16, prow, r);
+        convert_block_general<false>(s2, 2, sb2, alpha, beta, mul16, prow, r);
+        convert_block_general<false>(s3, 3, sb3, alpha, beta, mul16, prow, r);
     }
-    return static_cast<uint32_t>(X0 + 127) | (static_cast<uint32_t>(X1 + 127) << 8) |
-           (static_cast<uint32_t>(X2 + 127) << 16) | (static_cast<uint32_t>(X3 + 127) << 24);
+    // four bytes < 256 into one word
+    return (static_cast<uint32_t>(sb0) + static_cast<uint32_t>(sb1) * mul8) +
+           (static_cast<uint32_t>(sb2) + static_cast<uint32_t>(sb3) * mul8) * mul16;
 }
 
 // Per-row state of a softmax thread.
@@ -332,7 +334,10 @@ struct RowState {
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
-// then the two-stage conversion into P buffer wg.  false = aborted.
+// then the two-stage conversion into P buffer t % 4.  A wait that gives up
+// lets the tile run to its end on whatever the buffers hold (nothing is
+// read or written out of bounds); the warp-wide result, false = aborted,
+// ends the loop.
 template <bool kE4M3, bool kTail>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
@@ -340,13 +345,22 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     const int D = p.D;
     const int pb = t & (kPBuf - 1);
     uint8_t* const prow = sm.p[pb] + (r >> 3) * 1024 + (r & 7) * 128;
-    if (!wait_warp(&sm.s_full[wg], it & 1, p, sm)) return false;
+    bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
     tc_fence_after();
     uint32_t s0[32], s1[32], s2[32], s3[32];
     tmem_ld32(s_col, s0);
     tmem_ld32(s_col + 32, s1);
     tmem_ld32(s_col + 64, s2);
     tmem_ld32(s_col + 96, s3);
+    // while the scores travel: non-blocking looks at the other warpgroup's
+    // maximum of tile t - 1 and at this tile's P buffer (PV of tile t - 4
+    // retired); both are normally complete by now
+    const int ms = (t - 1) & 7;
+    const uint32_t m_par = ((t - 1) >> 3) & 1;
+    const uint32_t pf_par = ((t / kPBuf) - 1) & 1;
+    const bool have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
+    float prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
+    const bool have_p = t < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
     tmem_ld_wait();
     tmem_reg_dep(s0);
     tmem_reg_dep(s1);
@@ -378,8 +392,10 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     // frozen reference: replay the gate over the previous tile's maximum,
     // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
     if (t > 0) {
-        if (!wait_warp(&sm.m_ready[(t - 1) & 7], ((t - 1) >> 3) & 1, p, sm)) return false;
-        const float prev = sm.tmax_x[(t - 1) & 7][r];
+        if (!have_prev) {
+            ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
+            prev = sm.tmax_x[ms][r];
+        }
         if (t == 1 || (prev - rs.m_acc) * p.sm_scale > p.theta) rs.m_acc = prev;
     }
     bool fire = false;
@@ -396,12 +412,12 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     // P buffer pb is free once PV of tile t - 4 retired.  Waited first: PV
     // products retire in order, so afterwards the barrier of tile t - 1's
     // buffer can only be in the phase of PV_{t-1} itself.
-    if (t >= kPBuf && !wait_warp(&sm.p_free[pb], ((t / kPBuf) - 1) & 1, p, sm)) return false;
+    if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
     if (__any_sync(0xFFFFFFFFu, fire)) {
         // recovery: once PV of the previous tile retired, O and l of the
         // firing rows are scaled by exp(m_old - m_new) in TMEM
         const int pp = (t - 1) & (kPBuf - 1);
-        if (!wait_warp(&sm.p_free[pp], ((t - 1) / kPBuf) & 1, p, sm)) return false;
+        ok &= mbar_wait(&sm.p_free[pp], ((t - 1) / kPBuf) & 1, p.timeout_ns, &sm.abort);
         tc_fence_after();
         uint32_t rr[32];
         for (int c = 0; c < D / 32; ++c) {
@@ -418,13 +434,13 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
         tmem_st_wait();
     }
-    const uint32_t sfw =
-        convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc, prow, r);
+    const uint32_t sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha,
+                                             16249.0f - p.alpha * rs.m_acc, p.mul8, p.mul16, prow, r);
     tc_fence_before();
     *reinterpret_cast<uint32_t*>(sm.p_sf[pb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
     fence_async_smem();
     warp_arrive(&sm.p_full[pb]);
-    return true;
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
 template <bool kE4M3>
@@ -729,6 +745,8 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.theta = a.threshold;
     p.timeout_ns = a.timeout_ns;
     p.debug_flags = a.debug_flags;
+    p.mul8 = 1u << 8;
+    p.mul16 = 1u << 16;
     const size_t smem = sizeof(Smem);
     // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4
     auto kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<true> : fsa_attn_fwd_kernel<false>;
