@@ -48,7 +48,7 @@ namespace fsa {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kPBuf = 4;  // P buffers: tile t uses t % 4 (two per warpgroup)
+constexpr int kPBuf = 2;  // P buffers in TMEM: tile t uses t % 2 (one per warpgroup)
 constexpr int kThreads = 384;  // 2 softmax warpgroups + (K loader, MMA, V loader, spare)
 constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpLoadV = 10, kWarpPv = 11;
 // Register split: launched at 168 per thread (384 x 168 = 64512), the helper
@@ -61,17 +61,19 @@ constexpr int kTileBytes = 128 * 128;  // one 128 x 128 byte operand tile
 constexpr int kVBytes = kTileBytes + 16 * 128;  // V^T tile + 16 all-ones rows (row sums)
 constexpr uint32_t kTmemCols = 512;
 // TMEM column map: S0, S1 (128 each), O (D columns) with l in column D of
-// the same accumulator, and the scale-factor atoms (4 columns per atom)
+// the same accumulator (D + 16 columns written), P0, P1 (32 each: 128 E4M3
+// bytes per row), and the scale-factor atoms (4 columns per atom)
 constexpr uint32_t kColS0 = 0, kColO = 256;  // S1 = kColS0 + 128, l = kColO + D
-constexpr uint32_t kColSfQ = 416, kColSfK = 420 /* +4*(t&1) */, kColSfP = 428 /* +4*(t%4) */,
-                   kColSfV = 444 /* +8*(u&1): V rows 0-127, then unit scales for rows 128-255 */;
+constexpr uint32_t kColP = 400;              // + 32 * (t & 1)
+constexpr uint32_t kColSfQ = 464, kColSfK = 468 /* +4*(t&1) */, kColSfP = 476 /* +4*(t&1) */,
+                   kColSfV = 484 /* +8*(u&1): V rows 0-127, then unit scales for rows 128-255 */;
+static_assert(kColSfV + 16 <= 512, "TMEM column map beyond the allocation");
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic holds rne(x) in its low bits
 
 struct __align__(1024) Smem {
     uint8_t q[kTileBytes];
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kVBytes];  // rows [0, D): V^T tile; rows [D, D+16): all ones
-    uint8_t p[kPBuf][kTileBytes];
     uint8_t q_sf[kAtomBytes];
     uint8_t k_sf[kStages][kAtomBytes];
     uint8_t v_sf[kStages][kAtomBytes];
@@ -86,7 +88,7 @@ struct __align__(1024) Smem {
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_full[kPBuf];
-    uint64_t p_free[kPBuf];  // PV of the tile that used P buffer i retired
+    uint64_t p_free[kPBuf];  // PV of the tile that used P buffer i (and its scales) retired
     uint64_t m_ready[8]; // slot i of tmax_x written (tiles i, i + 8, ...)
     uint64_t o_full;
     uint64_t drain_qk, drain_pv;
@@ -237,11 +239,6 @@ __device__ __forceinline__ int block_scale_byte(float bmax, float alpha, float b
     return max((c + 127 - static_cast<int>(T::kMthr) - 128 * T::kEmax) >> 7, 0) + T::kOff;
 }
 
-__device__ __forceinline__ void store_p_block(uint8_t* prow, int r, int b, const uint32_t (&w)[8]) {
-    *reinterpret_cast<uint4*>(prow + (((2 * b) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(prow + (((2 * b + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
 // E4M3 P: the whole block converts to E4M3 normals when its smallest code is
 // a normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6), with
 // X = sb - 127.  Compared on the FP32 patterns of y + kMagic (signed, so a
@@ -251,15 +248,8 @@ __device__ __forceinline__ bool block_is_linear(float bn, int sb, float alpha, f
     return cmin >= kMagicBits + 128 * max(sb - 6, 1);
 }
 
-// The general conversion of one block (subnormal P elements, clamped codes);
-// inv = 2^-X with X = sb - 127.
-template <bool kClamp>
-__device__ __forceinline__ void convert_block_general(const uint32_t (&v)[32], int b, int sb, float alpha,
-                                                      float beta, uint32_t mul16, uint8_t* prow, int r) {
-    uint32_t w[8];
-    convert32<kClamp>(v, alpha, beta, __int_as_float((254 - sb) << 23), mul16, w);
-    store_p_block(prow, r, b, w);
-}
+// inv = 2^-X of the general conversion, X = sb - 127
+__device__ __forceinline__ float general_inv(int sb) { return __int_as_float((254 - sb) << 23); }
 
 // kx = 188728320 - 128 X: one unit of X is 8 units in the last place of a
 // float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f; with X = sb - 127
@@ -279,14 +269,16 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
 }
 
 // The two-stage conversion of a whole tile for row r (four 32-key blocks):
-// block scales from the block maxima, then E4M3 patterns into the P row.
-// Returns the four E8M0 scale bytes packed into a word.
+// block scales from the block maxima, then the E4M3 patterns of the row in
+// w0..w3 (keys 32 b .. 32 b + 31 in w_b).  Returns the four E8M0 scale bytes
+// packed into a word.
 template <bool kE4M3>
 __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
                                                  const uint32_t (&s2)[32], const uint32_t (&s3)[32],
                                                  const float (&bmax)[4], const float (&bmin)[4],
                                                  float alpha, float beta, uint32_t mul8, uint32_t mul16,
-                                                 uint8_t* prow, int r) {
+                                                 uint32_t (&w0)[8], uint32_t (&w1)[8], uint32_t (&w2)[8],
+                                                 uint32_t (&w3)[8]) {
     const int sb0 = block_scale_byte<kE4M3>(bmax[0], alpha, beta);
     const int sb1 = block_scale_byte<kE4M3>(bmax[1], alpha, beta);
     const int sb2 = block_scale_byte<kE4M3>(bmax[2], alpha, beta);
@@ -297,28 +289,23 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
                                              block_is_linear(bmin[1], sb1, alpha, beta) &&
                                              block_is_linear(bmin[2], sb2, alpha, beta) &&
                                              block_is_linear(bmin[3], sb3, alpha, beta))) {
-        uint32_t w0[8], w1[8], w2[8], w3[8];
         convert32_linear(s0, alpha, beta, linear_kx(sb0), mul8, w0);
         convert32_linear(s1, alpha, beta, linear_kx(sb1), mul8, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), mul8, w2);
         convert32_linear(s3, alpha, beta, linear_kx(sb3), mul8, w3);
-        store_p_block(prow, r, 0, w0);
-        store_p_block(prow, r, 1, w1);
-        store_p_block(prow, r, 2, w2);
-        store_p_block(prow, r, 3, w3);
     } else if (kE4M3 || __any_sync(0xFFFFFFFFu,
                                    __fmaf_rn(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
                                              alpha, beta) < 0.0f)) {
         // some weight of the warp's rows clamps to zero
-        convert_block_general<true>(s0, 0, sb0, alpha, beta, mul16, prow, r);
-        convert_block_general<true>(s1, 1, sb1, alpha, beta, mul16, prow, r);
-        convert_block_general<true>(s2, 2, sb2, alpha, beta, mul16, prow, r);
-        convert_block_general<true>(s3, 3, sb3, alpha, beta, mul16, prow, r);
+        convert32<true>(s0, alpha, beta, general_inv(sb0), mul16, w0);
+        convert32<true>(s1, alpha, beta, general_inv(sb1), mul16, w1);
+        convert32<true>(s2, alpha, beta, general_inv(sb2), mul16, w2);
+        convert32<true>(s3, alpha, beta, general_inv(sb3), mul16, w3);
     } else {
-        convert_block_general<false>(s0, 0, sb0, alpha, beta, mul16, prow, r);
-        convert_block_general<false>(s1, 1, sb1, alpha, beta, mul16, prow, r);
-        convert_block_general<false>(s2, 2, sb2, alpha, beta, mul16, prow, r);
-        convert_block_general<false>(s3, 3, sb3, alpha, beta, mul16, prow, r);
+        convert32<false>(s0, alpha, beta, general_inv(sb0), mul16, w0);
+        convert32<false>(s1, alpha, beta, general_inv(sb1), mul16, w1);
+        convert32<false>(s2, alpha, beta, general_inv(sb2), mul16, w2);
+        convert32<false>(s3, alpha, beta, general_inv(sb3), mul16, w3);
     }
     // four bytes < 256 into one word
     return (static_cast<uint32_t>(sb0) + static_cast<uint32_t>(sb1) * mul8) +
@@ -334,17 +321,16 @@ struct RowState {
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
-// then the two-stage conversion into P buffer t % 4.  A wait that gives up
+// then the two-stage conversion into TMEM P buffer t % 2.  A wait that gives up
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
-template <bool kE4M3, bool kTail>
+template <bool kE4M3>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
-                                             bool row_valid, int64_t grow, RowState& rs) {
+                                             bool row_valid, int64_t grow, bool tail, RowState& rs) {
     const int D = p.D;
     const int pb = t & (kPBuf - 1);
-    uint8_t* const prow = sm.p[pb] + (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
     tc_fence_after();
     uint32_t s0[32], s1[32], s2[32], s3[32];
@@ -353,11 +339,11 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tmem_ld32(s_col + 64, s2);
     tmem_ld32(s_col + 96, s3);
     // while the scores travel: non-blocking looks at the other warpgroup's
-    // maximum of tile t - 1 and at this tile's P buffer (PV of tile t - 4
+    // maximum of tile t - 1 and at this tile's P buffer (PV of tile t - 2
     // retired); both are normally complete by now
     const int ms = (t - 1) & 7;
     const uint32_t m_par = ((t - 1) >> 3) & 1;
-    const uint32_t pf_par = ((t / kPBuf) - 1) & 1;
+    const uint32_t pf_par = ((t >> 1) - 1) & 1;
     const bool have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
     float prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
     const bool have_p = t < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
@@ -369,8 +355,8 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     // the whole tile is in registers: the next score product may reuse S
     tc_fence_before();
     warp_arrive(&sm.s_free[wg]);
-    if (kTail) {
-        // keys >= S are masked before the gate and the conversion
+    if (tail) {
+        // keys >= S of a partial last tile are masked before the gate and the conversion
         const int n_valid = p.S - t * kTile;
         mask32(s0, n_valid);
         mask32(s1, n_valid - 32);
@@ -409,15 +395,15 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     }
     if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
     rs.fired += (fire && row_valid) ? 1u : 0u;
-    // P buffer pb is free once PV of tile t - 4 retired.  Waited first: PV
+    // P buffer pb is free once PV of tile t - 2 retired.  Waited first: PV
     // products retire in order, so afterwards the barrier of tile t - 1's
-    // buffer can only be in the phase of PV_{t-1} itself.
+    // buffer is past PV_{t-3} and can only be in the phase of PV_{t-1}
+    // itself (PV_{t+1} needs this tile's P).
     if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
     if (__any_sync(0xFFFFFFFFu, fire)) {
         // recovery: once PV of the previous tile retired, O and l of the
         // firing rows are scaled by exp(m_old - m_new) in TMEM
-        const int pp = (t - 1) & (kPBuf - 1);
-        ok &= mbar_wait(&sm.p_free[pp], ((t - 1) / kPBuf) & 1, p.timeout_ns, &sm.abort);
+        ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
         tc_fence_after();
         uint32_t rr[32];
         for (int c = 0; c < D / 32; ++c) {
@@ -434,11 +420,17 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
         tmem_st_wait();
     }
+    uint32_t w0[8], w1[8], w2[8], w3[8];
     const uint32_t sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha,
-                                             16249.0f - p.alpha * rs.m_acc, p.mul8, p.mul16, prow, r);
-    tc_fence_before();
+                                             16249.0f - p.alpha * rs.m_acc, p.mul8, p.mul16,
+                                             w0, w1, w2, w3);
+    // the P row into TMEM (the A operand of the PV product), its scales into
+    // the shared-memory atom the PV issuer copies to TMEM
+    tmem_st32(lane_addr + kColP + 32 * pb, w0, w1, w2, w3);
     *reinterpret_cast<uint32_t*>(sm.p_sf[pb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
     fence_async_smem();
+    tmem_st_wait();
+    tc_fence_before();
     warp_arrive(&sm.p_full[pb]);
     return __all_sync(0xFFFFFFFFu, ok);
 }
@@ -615,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, SWZ_128B);
-                const uint64_t dp0 = smem_desc(smem_u32(sm.p[0]), 16, 1024, SWZ_128B);
                 const uint64_t sfv0 = smem_desc(smem_u32(sm.v_sf[0]), 0, 128, SWZ_NONE);
                 const uint64_t sfp0 = smem_desc(smem_u32(sm.p_sf[0]), 0, 128, SWZ_NONE);
                 const uint32_t id_pv = idesc_mxf8f6f4(128, D + 16, 0, 0, 0, 0);
@@ -626,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int st = 0;  // V ring stage of tile u
                 for (int u = 0; ok && u < p.n_t; ++u) {
                     const int pb = u & (kPBuf - 1);
-                    if (!mbar_wait(&sm.p_full[pb], (u / kPBuf) & 1, p.timeout_ns, &sm.abort) ||
+                    if (!mbar_wait(&sm.p_full[pb], (u >> 1) & 1, p.timeout_ns, &sm.abort) ||
                         !mbar_wait(&sm.v_full[st], (u / kStages) & 1, p.timeout_ns, &sm.abort)) {
                         ok = false;
                         break;
@@ -635,12 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sfa = tmem + kColSfP + 4 * pb, sfb = tmem + kColSfV + 8 * (u & 1);
                     tc_cp_32x128b_x4(sfa, sfp0 + kAtomUnits * pb);
                     tc_cp_32x128b_x4(sfb, sfv0 + kAtomUnits * st);
-                    const uint64_t ap = dp0 + kStageUnits * pb, bv = dv0 + kVUnits * st;
+                    // A = P from TMEM: 8 columns per 32-key step
+                    const uint32_t ap = tmem + kColP + 32 * pb;
+                    const uint64_t bv = dv0 + kVUnits * st;
                     const uint32_t acc = u > 0 ? 1u : 0u;
-                    mma_mxf8f6f4(tmem + kColO, ap, bv, id_pv | FSA_SF(0), sfa, sfb, acc);
-                    mma_mxf8f6f4(tmem + kColO, ap + 2, bv + 2, id_pv | FSA_SF(1), sfa, sfb, 1u);
-                    mma_mxf8f6f4(tmem + kColO, ap + 4, bv + 4, id_pv | FSA_SF(2), sfa, sfb, 1u);
-                    mma_mxf8f6f4(tmem + kColO, ap + 6, bv + 6, id_pv | FSA_SF(3), sfa, sfb, 1u);
+                    mma_mxf8f6f4_tmem_a(tmem + kColO, ap, bv, id_pv | FSA_SF(0), sfa, sfb, acc);
+                    mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 8, bv + 2, id_pv | FSA_SF(1), sfa, sfb, 1u);
+                    mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 16, bv + 4, id_pv | FSA_SF(2), sfa, sfb, 1u);
+                    mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 24, bv + 6, id_pv | FSA_SF(3), sfa, sfb, 1u);
                     tc_commit(&sm.v_empty[st]);
                     tc_commit(&sm.p_free[pb]);
                     st = st + 1 == kStages ? 0 : st + 1;
@@ -672,11 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         RowState rs{0.0f, 0u};
         bool ok = true;
         const int t_tail = (p.S % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
-        for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it) {
-            ok = (t == t_tail)
-                     ? softmax_tile<kE4M3, true>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, rs)
-                     : softmax_tile<kE4M3, false>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, rs);
-        }
+        for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
+            ok = softmax_tile<kE4M3>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
             ok = wait_warp(&sm.o_full, 0, p, sm);
