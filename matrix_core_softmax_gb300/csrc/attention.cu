@@ -77,7 +77,6 @@ struct __align__(1024) Smem {
     uint8_t q_sf[kAtomBytes];
     uint8_t k_sf[kStages][kAtomBytes];
     uint8_t v_sf[kStages][kAtomBytes];
-    uint8_t p_sf[kPBuf][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
     float tmax_x[8][128];  // row maxima of tile t in slot t % 8, read by the other warpgroup
     uint64_t bar_q;
@@ -424,11 +423,11 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     const uint32_t sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha,
                                              16249.0f - p.alpha * rs.m_acc, p.mul8, p.mul16,
                                              w0, w1, w2, w3);
-    // the P row into TMEM (the A operand of the PV product), its scales into
-    // the shared-memory atom the PV issuer copies to TMEM
+    // the P row into TMEM (the A operand of the PV product) and its four
+    // scale bytes where the product reads the scales of row r: lane r,
+    // column r / 32 of the P buffer's 4-column scale atom
     tmem_st32(lane_addr + kColP + 32 * pb, w0, w1, w2, w3);
-    *reinterpret_cast<uint32_t*>(sm.p_sf[pb] + (r & 31) * 16 + (r >> 5) * 4) = sfw;
-    fence_async_smem();
+    tmem_st1(lane_addr + kColSfP + 4 * pb + (r >> 5), sfw);
     tmem_st_wait();
     tc_fence_before();
     warp_arrive(&sm.p_full[pb]);
@@ -608,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, SWZ_128B);
                 const uint64_t sfv0 = smem_desc(smem_u32(sm.v_sf[0]), 0, 128, SWZ_NONE);
-                const uint64_t sfp0 = smem_desc(smem_u32(sm.p_sf[0]), 0, 128, SWZ_NONE);
                 const uint32_t id_pv = idesc_mxf8f6f4(128, D + 16, 0, 0, 0, 0);
                 // unit scales for PV B rows 128-255 (the all-ones rows when D = 128)
                 const uint64_t sf1 = smem_desc(smem_u32(sm.ones_sf), 0, 128, SWZ_NONE);
@@ -624,7 +622,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t sfa = tmem + kColSfP + 4 * pb, sfb = tmem + kColSfV + 8 * (u & 1);
-                    tc_cp_32x128b_x4(sfa, sfp0 + kAtomUnits * pb);
                     tc_cp_32x128b_x4(sfb, sfv0 + kAtomUnits * st);
                     // A = P from TMEM: 8 columns per 32-key step
                     const uint32_t ap = tmem + kColP + 32 * pb;
