@@ -52,9 +52,9 @@ constexpr int kPBuf = 2;  // P buffers in TMEM: tile t uses t % 2 (one per warpg
 constexpr int kThreads = 384;  // 2 softmax warpgroups + (K loader, MMA, V loader, spare)
 constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpLoadV = 10, kWarpPv = 11;
 // Register split: launched at 168 per thread (384 x 168 = 64512), the helper
-// warpgroup gives back to 48 and the softmax warpgroups take 224:
-// 2 * 128 * 224 + 128 * 48 = 63488 <= 64512.
-constexpr int kLaunchRegs = 168, kSoftmaxRegs = 224, kHelperRegs = 48;
+// warpgroup gives back to 32 and the softmax warpgroups take 232:
+// 2 * 128 * 232 + 128 * 32 = 63488 <= 64512.
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 232, kHelperRegs = 32;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kTileBytes = 128 * 128;  // one 128 x 128 byte operand tile
