@@ -109,6 +109,7 @@ struct Params {
     float sm_scale;  // s = sm_scale * accumulator
     float alpha;     // 128 * log2(e) * sm_scale
     float theta;     // gate threshold, natural-log score units
+    float theta_raw; // theta / sm_scale: the same threshold on accumulator values
     uint64_t timeout_ns;
     int debug_flags;
     // 2^8 and 2^16, held in registers: byte and half-word packing as an
@@ -238,8 +239,8 @@ __device__ __forceinline__ int block_scale_byte(float bmax, float alpha, float b
     return max((c + 127 - static_cast<int>(T::kMthr) - 128 * T::kEmax) >> 7, 0) + T::kOff;
 }
 
-// E4M3 P: the whole block converts to E4M3 normals when its smallest code is
-// a normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6), with
+// E4M3 P: a block converts to E4M3 normals when its smallest code is a
+// normal bf16 (>= 128) and at least 128 X + 15488 (p / 2^X >= 2^-6), with
 // X = sb - 127.  Compared on the FP32 patterns of y + kMagic (signed, so a
 // negative y fails).
 __device__ __forceinline__ bool block_is_linear(float bn, int sb, float alpha, float beta) {
@@ -282,12 +283,13 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
     const int sb1 = block_scale_byte<kE4M3>(bmax[1], alpha, beta);
     const int sb2 = block_scale_byte<kE4M3>(bmax[2], alpha, beta);
     const int sb3 = block_scale_byte<kE4M3>(bmax[3], alpha, beta);
-    // one decision for the whole tile: every block of every row of the warp
-    // converts linearly (the common case for MXFP8), else block by block
-    if (kE4M3 && __all_sync(0xFFFFFFFFu, block_is_linear(bmin[0], sb0, alpha, beta) &&
-                                             block_is_linear(bmin[1], sb1, alpha, beta) &&
-                                             block_is_linear(bmin[2], sb2, alpha, beta) &&
-                                             block_is_linear(bmin[3], sb3, alpha, beta))) {
+    // one decision for the whole tile: every row of the warp converts
+    // linearly (the common case for MXFP8), else block by block.  Checked
+    // once per row against the largest block threshold (sb grows with the
+    // block maximum), which implies every block's own condition.
+    if (kE4M3 && __all_sync(0xFFFFFFFFu,
+                            block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                            max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
         convert32_linear(s0, alpha, beta, linear_kx(sb0), mul8, w0);
         convert32_linear(s1, alpha, beta, linear_kx(sb1), mul8, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), mul8, w2);
@@ -381,25 +383,28 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
             prev = sm.tmax_x[ms][r];
         }
-        if (t == 1 || (prev - rs.m_acc) * p.sm_scale > p.theta) rs.m_acc = prev;
+        if (t == 1 || prev - rs.m_acc > p.theta_raw) rs.m_acc = prev;
     }
     bool fire = false;
     float rescale = 1.0f;
     if (t == 0) {
         rs.m_acc = tmax;
-    } else if ((tmax - rs.m_acc) * p.sm_scale > p.theta) {
+    } else if (tmax - rs.m_acc > p.theta_raw) {
         fire = true;
         rescale = expf((rs.m_acc - tmax) * p.sm_scale);
         rs.m_acc = tmax;
     }
-    if (p.rollback_bits && row_valid) p.rollback_bits[grow * p.n_t + t] = fire ? 1 : 0;
-    rs.fired += (fire && row_valid) ? 1u : 0u;
     // P buffer pb is free once PV of tile t - 2 retired.  Waited first: PV
     // products retire in order, so afterwards the barrier of tile t - 1's
     // buffer is past PV_{t-3} and can only be in the phase of PV_{t-1}
     // itself (PV_{t+1} needs this tile's P).
     if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
     if (__any_sync(0xFFFFFFFFu, fire)) {
+        // the bitmap was zeroed before the launch: only firings are written
+        if (fire && row_valid) {
+            if (p.rollback_bits) p.rollback_bits[grow * p.n_t + t] = 1;
+            ++rs.fired;
+        }
         // recovery: once PV of the previous tile retired, O and l of the
         // firing rows are scaled by exp(m_old - m_new) in TMEM
         ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
@@ -522,24 +527,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
             int issued = 0;
             bool ok = true;
+            int st = 0;            // ring stage of tile t
+            uint32_t ph = 0;       // parity of the ring's current pass
             for (int t = 0; t < p.n_t; ++t) {
-                const int st = t % kStages;
-                if (t >= kStages &&
-                    !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, p.timeout_ns, &sm.abort)) {
+                if (t >= kStages && !mbar_wait(&empty[st], ph ^ 1u, p.timeout_ns, &sm.abort)) {
                     ok = false;
                     break;
                 }
-                if (is_k && (p.debug_flags & 1) && t == 1) continue;  // test: K tile 1 never arrives
-                mbar_arrive_expect_tx(&full[st], tile_bytes + kAtomBytes);
-                const int64_t a = (static_cast<int64_t>(bh) * p.n_t + t) * kAtomBytes;
-                if (is_k) {
-                    tma_load_3d(sm.k[st], &tm_k, &full[st], 0, t * kTile, bh);
-                    bulk_load(sm.k_sf[st], p.k_sf + a, kAtomBytes, &full[st]);
-                } else {
-                    tma_load_3d(sm.v[st], &tm_v, &full[st], t * kTile, 0, bh);
-                    bulk_load(sm.v_sf[st], p.v_sf + a, kAtomBytes, &full[st]);
+                // test hook: K tile 1 never arrives
+                if (!(is_k && (p.debug_flags & 1) && t == 1)) {
+                    mbar_arrive_expect_tx(&full[st], tile_bytes + kAtomBytes);
+                    const int64_t a = (static_cast<int64_t>(bh) * p.n_t + t) * kAtomBytes;
+                    if (is_k) {
+                        tma_load_3d(sm.k[st], &tm_k, &full[st], 0, t * kTile, bh);
+                        bulk_load(sm.k_sf[st], p.k_sf + a, kAtomBytes, &full[st]);
+                    } else {
+                        tma_load_3d(sm.v[st], &tm_v, &full[st], t * kTile, 0, bh);
+                        bulk_load(sm.v_sf[st], p.v_sf + a, kAtomBytes, &full[st]);
+                    }
                 }
                 issued = t + 1;
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
             if (!ok) raise_abort(sm, p);
             if (sm.abort) {
@@ -730,6 +741,7 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.sm_scale = a.sm_scale;
     p.alpha = static_cast<float>(128.0 * 1.4426950408889634 * static_cast<double>(a.sm_scale));
     p.theta = a.threshold;
+    p.theta_raw = a.threshold / a.sm_scale;
     p.timeout_ns = a.timeout_ns;
     p.debug_flags = a.debug_flags;
     p.mul8 = 1u << 8;

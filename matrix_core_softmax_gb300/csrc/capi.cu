@@ -203,6 +203,11 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int S, int D, int fmt, f
                    1000000ull;
     a.debug_flags = op.debug_flags;
     a.err_word = err;
+    // the kernel writes only the bytes of firings
+    if (op.rollback_bits &&
+        cudaMemsetAsync(op.rollback_bits, 0, static_cast<size_t>(BH) * S * ((S + kTile - 1) / kTile), st) !=
+            cudaSuccess)
+        return FSA_ERR_CUDA;
     return launch_fsa_attention(a, st) == cudaSuccess ? FSA_OK : FSA_ERR_CUDA;
 }
 
