@@ -15,24 +15,24 @@
 //     E8M0 scale and is converted to the P element type (two-stage
 //     conversion);
 //   * O += P^ V^ and l += P^ 1 come from one more block-scaled MMA on the
-//     same P^ in shared memory: the V^T operand carries 16 extra all-ones
-//     rows, so column D of the accumulator is the row sum;
+//     same P^, read from tensor memory: the V^T operand carries 16 extra
+//     all-ones rows, so column D of the accumulator is the row sum;
 //   * a row whose tile maximum passes its reference by more than theta
 //     rolls back: O and l are rescaled by exp(m_old - m_new) in TMEM and the
 //     reference moves to the tile maximum ("recovery procedure", paragraph 5).
 //
-// Work decomposition: one CTA per (128-row query tile, head); 10 warps:
-//   warps 0-3  softmax warpgroup 0: KV tiles 0, 2, 4, ... (S buffer 0, P buffers 0, 2)
-//   warps 4-7  softmax warpgroup 1: KV tiles 1, 3, 5, ... (S buffer 1, P buffers 1, 3)
+// Work decomposition: one CTA per (128-row query tile, head); 12 warps:
+//   warps 0-3  softmax warpgroup 0: KV tiles 0, 2, 4, ... (S buffer 0, P buffer 0)
+//   warps 4-7  softmax warpgroup 1: KV tiles 1, 3, 5, ... (S buffer 1, P buffer 1)
 //              thread r of a warpgroup owns query row r = TMEM lane r; the
-//              frozen reference is handed from one warpgroup to the other
-//              after every tile (shared memory + mbarrier);
+//              tile maxima are handed from one warpgroup to the other
+//              (shared memory + mbarrier) and each replays the gate;
 //   warp 8     TMA producer of Q and the K ring; warp 10 of the V^T ring;
 //   warp 9     TMEM allocator and issuer of the score products;
-//   warp 11    issuer of the PV products (four P buffers in shared memory).
-// QK^T of tile t+1 runs while tile t is converted, and each scheduler holds
-// two softmax warps.  Each tile is read from TMEM twice: pass 1 takes the
-// 32-key block maxima/minima (gate, block scales), pass 2 converts.
+//   warp 11    issuer of the PV products.
+// The score product of tile t+1 runs while tile t is converted, and each
+// scheduler holds two softmax warps.  Each tile's scores are read from TMEM
+// once; P and its scale bytes go back to TMEM with tcgen05.st.
 //
 // MMA operands are E4M3 bit patterns for all three formats: every E2M3 and
 // E2M1 value is exactly an E4M3 value, kind::mxf8f6f4 runs at one rate for
