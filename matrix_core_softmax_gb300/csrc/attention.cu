@@ -198,21 +198,27 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, 
 // + kx (= 1.5 * 2^27 - 1.5 * 2^23 - 15360 - 128 X, a multiple of 16) lands
 // in [2^27, 2^28) where one unit in the last place is 16, rounding the
 // quotient to nearest even; its pattern is 0x4D400000 + the E4M3 code.
-// Packing: the pattern's low 16 bits are the code alone, so
-// pattern_1 * 2^8 + pattern_0 holds codes 0 and 1 in its low half-word.
+// Packing four codes c0..c3 with integer multiply-adds only (FMA pipe):
+// lo = pat1 * 2^8 + pat0 = 0x8D400000 + (c1 c0); element 2 is converted
+// with kx - 16 * 0x8D40 (a multiple of 16 in the same binade, so the same
+// rounding) and so has the pattern 0x4D400000 - 0x8D40 + c2, which makes
+// hi = pat3 * 2^8 + pat2 = (c3 c2) - 0x8D40 (mod 2^16) in its low half;
+// hi * 2^16 + lo = (c3 c2 c1 c0) exactly (mod 2^32).
 __device__ __forceinline__ void convert32_linear(const uint32_t (&v)[32], float alpha, float beta,
-                                                 float kx, uint32_t mul8, uint32_t (&w)[8]) {
+                                                 float kx, float kx2, uint32_t mul8, uint32_t mul16,
+                                                 uint32_t (&w)[8]) {
     const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
-    const float2 m2 = make_float2(kMagic, kMagic), k2 = make_float2(kx, kx);
+    const float2 m2 = make_float2(kMagic, kMagic);
+    const float2 k01 = make_float2(kx, kx), k23 = make_float2(kx2, kx);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float2 y0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), a2, b2);
         float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), a2, b2);
-        y0 = __fadd2_rn(__fadd2_rn(y0, m2), k2);
-        y1 = __fadd2_rn(__fadd2_rn(y1, m2), k2);
+        y0 = __fadd2_rn(__fadd2_rn(y0, m2), k01);
+        y1 = __fadd2_rn(__fadd2_rn(y1, m2), k23);
         const uint32_t lo = __float_as_uint(y0.y) * mul8 + __float_as_uint(y0.x);
         const uint32_t hi = __float_as_uint(y1.y) * mul8 + __float_as_uint(y1.x);
-        w[i] = __byte_perm(lo, hi, 0x5410);
+        w[i] = hi * mul16 + lo;
     }
 }
 
@@ -255,6 +261,8 @@ __device__ __forceinline__ float general_inv(int sb) { return __int_as_float((25
 // float in [2^27, 2^28), and 0x4D33FC40 is 188728320.0f; with X = sb - 127
 // the pattern is 0x4D340038 - 8 sb.
 __device__ __forceinline__ float linear_kx(int sb) { return __int_as_float(0x4D340038 - 8 * sb); }
+// kx - 16 * 0x8D40 (the packing offset of every fourth element)
+__device__ __forceinline__ float linear_kx2(int sb) { return __int_as_float(0x4D3372F8 - 8 * sb); }
 
 // One arrival per warp: the lanes' preceding shared-memory writes and TMEM
 // reads are ordered before lane 0's release-arrive by the warp barrier.
@@ -290,10 +298,10 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
     if (kE4M3 && __all_sync(0xFFFFFFFFu,
                             block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
                                             max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
-        convert32_linear(s0, alpha, beta, linear_kx(sb0), mul8, w0);
-        convert32_linear(s1, alpha, beta, linear_kx(sb1), mul8, w1);
-        convert32_linear(s2, alpha, beta, linear_kx(sb2), mul8, w2);
-        convert32_linear(s3, alpha, beta, linear_kx(sb3), mul8, w3);
+        convert32_linear(s0, alpha, beta, linear_kx(sb0), linear_kx2(sb0), mul8, mul16, w0);
+        convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
+        convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
+        convert32_linear(s3, alpha, beta, linear_kx(sb3), linear_kx2(sb3), mul8, mul16, w3);
     } else if (kE4M3 || __any_sync(0xFFFFFFFFu,
                                    __fmaf_rn(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
                                              alpha, beta) < 0.0f)) {
