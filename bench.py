@@ -10,6 +10,7 @@ kernel alone; `e2e` repeats the step through the public C-ABI call with the
 inputs copied in from pinned host memory and the outputs copied back.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py --schedule    # 20-step hybrid MXFP6/MXFP4 schedule vs all-BF16 / all-MXFP4
 """
 from __future__ import annotations
 
@@ -187,6 +188,58 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_schedules(args, w, fsa, tq, tk, tv, o, ws, stream, dev, rank):
+    """Attention time of whole denoising schedules: every step is one library
+    call on the step's format (quantization + fused kernel for MX formats,
+    the BF16 kernel for bf16), timed with CUDA events around each call.  The
+    inputs are the same synthetic tensors every step."""
+    from matrix_core_softmax_gb300 import schedule as sch
+    plans = {
+        "hybrid": sch.hybrid_schedule(),
+        "all-mxfp4": sch.uniform_schedule("mxfp4"),
+        "all-mxfp6": sch.uniform_schedule("mxfp6"),
+        "all-mxfp8": sch.uniform_schedule("mxfp8"),
+        "all-bf16": sch.uniform_schedule("bf16"),
+    }
+    for fmt in sch.STEP_FORMATS:  # warm-up: one call of every format
+        for _ in range(max(1, args.warmup)):
+            sch.attention_step(tq, tk, tv, fmt, THRESHOLD, out=o, workspace=ws)
+    torch.cuda.synchronize(dev)
+    if fsa.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    res = {}
+    with ClockSampler(int(dev.index or 0)) as clk:
+        for name, plan in plans.items():
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(plan) + 1)]
+            ev[0].record(stream)
+            for i, fmt in enumerate(plan):
+                sch.attention_step(tq, tk, tv, fmt, THRESHOLD, out=o, workspace=ws)
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            per = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(plan))]
+            res[name] = {"formats": plan, "total_ms": sum(per), "per_step_ms": per}
+    st = fsa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error: {fsa.status_string(st)}")
+    if rank != 0:
+        return
+    hyb = res["hybrid"]["total_ms"]
+    line = {
+        "metric": "self-attention time of a 20-step video-DiT denoising schedule",
+        "value": hyb, "unit": "ms", "higher_is_better": False, "n_gpus": 1,
+        "data": "synthetic N(0,1) bf16, the same Q, K, V every step",
+        "config": {"workload": workload_name(args.workload, w), "threshold": THRESHOLD,
+                   "steps": len(plans["hybrid"]),
+                   "hybrid": "MXFP6 for steps 0-2 and 17-19, MXFP4 for steps 3-16",
+                   "per_step": "one library call: quantize Q,K,V + fused attention (MX), or the BF16 kernel"},
+        "schedules": res,
+        "speedup_hybrid_vs_all_bf16": res["all-bf16"]["total_ms"] / hyb,
+        "speedup_hybrid_vs_all_mxfp4": res["all-mxfp4"]["total_ms"] / hyb,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -199,6 +252,8 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=768)
     ap.add_argument("--ref-rows", type=int, default=96)
+    ap.add_argument("--schedule", action="store_true",
+                    help="time the 20-step hybrid precision schedule against all-BF16 and all-MXFP4")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
 
@@ -231,6 +286,9 @@ def main():
     ws = fsa.new_workspace(B, H, S, D, device=dev)
     stream = torch.cuda.current_stream(dev)
     F = flops(w)
+    if args.schedule:
+        run_schedules(args, w, fsa, tq, tk, tv, o, ws, stream, dev, rank)
+        return
 
     def step(ev=None):
         for i, fmt in enumerate(FORMATS):
