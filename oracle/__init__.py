@@ -90,6 +90,11 @@ def _load():
                                           ctypes.POINTER(_Params), P, ctypes.c_int64, ctypes.c_int,
                                           P, P, P, P, P, P, ctypes.POINTER(ctypes.c_int64)]
             lib.ora_attention.restype = ctypes.c_int
+            lib.ora_attention_qk.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int, ctypes.POINTER(_Params), P, ctypes.c_int64,
+                                             ctypes.c_int, P, P, P, P, P, P,
+                                             ctypes.POINTER(ctypes.c_int64)]
+            lib.ora_attention_qk.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -157,7 +162,8 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
               threshold: float = 8.0, tile: int = 128, sm_scale: float = 0.0,
               rows=None, threads: int | None = None, want_bits: bool = False,
               want_margins: bool = False):
-    """Oracle attention on bf16 bit patterns q/k/v[BH][S][D] (uint16).
+    """Oracle attention on bf16 bit patterns q[BH][Sq][D], k/v[BH][Sk][D]
+    (uint16; Sq = Sk for self-attention).
 
     mode:
       "fused"         -- the method: MX Q/K/V, frozen reference + gate,
@@ -169,7 +175,7 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
       "exact"         -- FP64 softmax attention on the bf16 inputs.
       "exact_frozen"  -- the method's frozen reference and gate with exact exp
                          and no quantization (equals "exact" for any theta).
-    rows: optional global row indices bh*S+i; outputs follow that order.
+    rows: optional global query-row indices bh*Sq+i; outputs follow that order.
     Returns a dict with "out" (float64 [n][D]), "out_bf16" (uint16),
     "m", "l", "rollback_count" and optionally "bits" / "margins" [n][n_t].
     """
@@ -180,7 +186,10 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
         q = q.reshape(-1, q.shape[-2], q.shape[-1])
         k = k.reshape(-1, k.shape[-2], k.shape[-1])
         v = v.reshape(-1, v.shape[-2], v.shape[-1])
-    BH, S, D = q.shape
+    BH, Sq, D = q.shape
+    S = k.shape[1]          # keys
+    if k.shape != (BH, S, D) or v.shape != (BH, S, D):
+        raise ValueError("k and v must be [BH][Sk][D] with q's BH and D")
     qkv_fmt, p_fmt = FORMATS[fmt] if fmt is not None else (-1, -1)
     p = _Params()
     p.tile, p.threshold, p.sm_scale = tile, float(threshold), float(sm_scale)
@@ -198,7 +207,7 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
         raise ValueError(mode)
     if rows is None:
         rows_arr = None
-        n = BH * S
+        n = BH * Sq
     else:
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         n = rows_arr.shape[0]
@@ -212,10 +221,10 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
     cnt = ctypes.c_int64(0)
     if threads is None:
         threads = len(os.sched_getaffinity(0))
-    rc = _load().ora_attention(_ptr(q), _ptr(k), _ptr(v), BH, S, D, ctypes.byref(p),
-                               _ptr(rows_arr), n, int(threads), _ptr(out), _ptr(out_bf16),
-                               _ptr(bits), _ptr(margins), _ptr(row_m), _ptr(row_l),
-                               ctypes.byref(cnt))
+    rc = _load().ora_attention_qk(_ptr(q), _ptr(k), _ptr(v), BH, Sq, S, D, ctypes.byref(p),
+                                  _ptr(rows_arr), n, int(threads), _ptr(out), _ptr(out_bf16),
+                                  _ptr(bits), _ptr(margins), _ptr(row_m), _ptr(row_l),
+                                  ctypes.byref(cnt))
     if rc != 0:
         raise ValueError(f"ora_attention failed ({rc})")
     res = {"out": out, "out_bf16": out_bf16, "m": row_m, "l": row_l,

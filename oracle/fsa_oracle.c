@@ -267,10 +267,10 @@ typedef struct {
 typedef struct {
     /* inputs */
     const uint16_t *q, *k, *v;
-    int64_t S;
+    int64_t Sq, Sk;             /* query rows and keys per head */
     int D;
     const ora_params *p;
-    const double *kd, *vd;      /* dequantized K[S][D] and V[S][D] of this head */
+    const double *kd, *vd;      /* dequantized K[Sk][D] and V[Sk][D] of this head */
     int64_t bh;                 /* head index (b*H + h) */
     const int64_t *rows;        /* row indices within the head */
     const int64_t *out_idx;     /* output slot of each row */
@@ -289,7 +289,7 @@ typedef struct {
 static int attention_row(ora_job *J, int64_t i, int64_t slot)
 {
     const ora_params *P = J->p;
-    const int64_t S = J->S;
+    const int64_t S = J->Sk;    /* keys */
     const int D = J->D;
     const int64_t n_t = (S + P->tile - 1) / P->tile;
     const double sm = P->sm_scale > 0.0 ? P->sm_scale : 1.0 / sqrt((double)D);
@@ -305,7 +305,7 @@ static int attention_row(ora_job *J, int64_t i, int64_t slot)
 
     /* Step 1: the query row, MX-quantized along D when quantization is on. */
     {
-        const uint16_t *qr = J->q + (J->bh * S + i) * D;
+        const uint16_t *qr = J->q + (J->bh * J->Sq + i) * D;
         for (d = 0; d < D; d++) qd[d] = ora_bf16_to_double(qr[d]);
         if (P->qkv_fmt >= 0)
             for (d = 0; d < D; d += 32)
@@ -435,28 +435,30 @@ static int prepare_head(const uint16_t *k, const uint16_t *v, int64_t bh, int64_
     return ORA_OK;
 }
 
-/* Attention over q,k,v [B*H][S][D] (bf16 bit patterns).
- * rows: global row indices bh*S + i to compute (n_rows of them, grouped by
- * head in any order), or NULL for every row (n_rows ignored).  Output slot r
- * holds the r-th requested row.  Outputs may be NULL.  bits/margins are
- * [n][n_t]; bits must be zeroed by the caller.  Returns the rollback count
- * through *rollback_count (may be NULL). */
-int ora_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                  int64_t BH, int64_t S, int D, const ora_params *p,
-                  const int64_t *rows, int64_t n_rows, int n_threads,
-                  double *out_f64, uint16_t *out_bf16, uint8_t *bits,
-                  double *margins, double *row_m, double *row_l,
-                  int64_t *rollback_count)
+/* Attention of q [B*H][Sq][D] over k, v [B*H][Sk][D] (bf16 bit patterns).
+ * rows: global query-row indices bh*Sq + i to compute (n_rows of them,
+ * grouped by head in any order), or NULL for every row (n_rows ignored).
+ * Output slot r holds the r-th requested row.  Outputs may be NULL.
+ * bits/margins are [n][n_t] with n_t = ceil(Sk / tile); bits must be zeroed
+ * by the caller.  Returns the rollback count through *rollback_count (may be
+ * NULL). */
+int ora_attention_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int64_t BH, int64_t Sq, int64_t Sk, int D, const ora_params *p,
+                     const int64_t *rows, int64_t n_rows, int n_threads,
+                     double *out_f64, uint16_t *out_bf16, uint8_t *bits,
+                     double *margins, double *row_m, double *row_l,
+                     int64_t *rollback_count)
 {
+    const int64_t S = Sk;
     int64_t bh, r, total = 0;
     int err = ORA_OK;
     int64_t *hrows = NULL, *hslot = NULL;
     double *kd = NULL, *vd = NULL;
-    if (!q || !k || !v || !p || BH < 0 || S < 1 || D < 1 || D > 256 || p->tile < 1 ||
+    if (!q || !k || !v || !p || BH < 0 || Sq < 1 || Sk < 1 || D < 1 || D > 256 || p->tile < 1 ||
         (p->qkv_fmt < -1 || p->qkv_fmt > 2) || (p->p_fmt < -1 || p->p_fmt > 2))
         return ORA_ERR_ARG;
     if (n_threads < 1) n_threads = 1;
-    if (!rows) n_rows = BH * S;
+    if (!rows) n_rows = BH * Sq;
     hrows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_rows + 1));
     hslot = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_rows + 1));
     kd = (double *)malloc(sizeof(double) * (size_t)(S * D));
@@ -470,8 +472,8 @@ int ora_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         int nt;
         for (r = 0; r < n_rows; r++) {
             int64_t g = rows ? rows[r] : r;
-            if (g < 0 || g >= BH * S) { err = ORA_ERR_ARG; goto done; }
-            if (g / S == bh) { hrows[nh] = g % S; hslot[nh] = r; nh++; }
+            if (g < 0 || g >= BH * Sq) { err = ORA_ERR_ARG; goto done; }
+            if (g / Sq == bh) { hrows[nh] = g % Sq; hslot[nh] = r; nh++; }
         }
         if (nh == 0) continue;
         prepare_head(k, v, bh, S, D, p->qkv_fmt, kd, vd);
@@ -482,7 +484,7 @@ int ora_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             ora_job *J = &jobs[w];
             int64_t a = w * per, b = a + per < nh ? a + per : nh;
             memset(J, 0, sizeof(*J));
-            J->q = q; J->k = k; J->v = v; J->S = S; J->D = D; J->p = p;
+            J->q = q; J->k = k; J->v = v; J->Sq = Sq; J->Sk = Sk; J->D = D; J->p = p;
             J->kd = kd; J->vd = vd; J->bh = bh;
             J->rows = hrows + a; J->out_idx = hslot + a; J->nrows = b > a ? b - a : 0;
             J->out_f64 = out_f64; J->out_bf16 = out_bf16; J->bits = bits;
@@ -500,4 +502,16 @@ done:
     if (rollback_count) *rollback_count = total;
     free(hrows); free(hslot); free(kd); free(vd);
     return err;
+}
+
+/* Self-attention: Sq = Sk = S. */
+int ora_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                  int64_t BH, int64_t S, int D, const ora_params *p,
+                  const int64_t *rows, int64_t n_rows, int n_threads,
+                  double *out_f64, uint16_t *out_bf16, uint8_t *bits,
+                  double *margins, double *row_m, double *row_l,
+                  int64_t *rollback_count)
+{
+    return ora_attention_qk(q, k, v, BH, S, S, D, p, rows, n_rows, n_threads, out_f64, out_bf16,
+                            bits, margins, row_m, row_l, rollback_count);
 }
