@@ -43,16 +43,42 @@ WORKLOADS = {
     "h32-s32768": dict(B=1, H=32, S=32768, D=128),
     "h32-s65536": dict(B=1, H=32, S=65536, D=128),
     "h32-s131072": dict(B=1, H=32, S=131072, D=128),
+    # head dim 64 at scale
+    "d64-h32-s32768": dict(B=1, H=32, S=32768, D=64),
+    # queries and keys of different lengths (S = query rows, Sk = keys): video
+    # tokens attending to a 512-token context, and a short query over a long one
+    "cross-q75600-k512": dict(B=1, H=40, S=75600, Sk=512, D=128),
+    "cross-q4096-k32768": dict(B=1, H=32, S=4096, Sk=32768, D=128),
 }
 THRESHOLD = 8.0
 
 
+def keys(w):
+    return w.get("Sk", w["S"])
+
+
+def is_cross(w):
+    return keys(w) != w["S"]
+
+
 def flops(w):
-    return 4.0 * w["B"] * w["H"] * w["S"] * w["S"] * w["D"]
+    return 4.0 * w["B"] * w["H"] * w["S"] * keys(w) * w["D"]
 
 
 def workload_name(name, w):
+    if is_cross(w):
+        return f"{name} B={w['B']} H={w['H']} Sq={w['S']} Sk={keys(w)} D={w['D']}"
     return f"{name} B={w['B']} H={w['H']} Sq=Sk={w['S']} D={w['D']}"
+
+
+def make_inputs(w, seed):
+    """Synthetic bf16 Q, K, V bit patterns; keys and values drawn separately
+    when their length differs from the queries'."""
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=seed, stress_from=w.get("stress_from"))
+    if is_cross(w):
+        _, k, v = fsa_inputs.qkv(B, H, keys(w), D, seed=seed + 1, stress_from=w.get("stress_from"))
+    return q, k, v
 
 
 def peaks():
@@ -151,14 +177,13 @@ def oracle_sample(q, k, v, w, fmt, n_rows, threads):
     oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=THRESHOLD, rows=rows,
                      threads=threads)
     dt = time.perf_counter() - t0
-    return n_rows * 4.0 * w["S"] * w["D"], dt
+    return n_rows * 4.0 * keys(w) * w["D"], dt
 
 
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
-    q, k, v = fsa_inputs.qkv(w["B"], w["H"], w["S"], w["D"], seed=0,
-                             stress_from=w.get("stress_from"))
+    q, k, v = make_inputs(w, 0)
     threads = len(os.sched_getaffinity(0))
     n_rows = args.ref_rows
     total_f, total_t = 0.0, 0.0
@@ -280,12 +305,16 @@ def main():
     fsa.load()
 
     B, H, S, D = w["B"], w["H"], w["S"], w["D"]
-    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=rank, stress_from=w.get("stress_from"))
+    Sk, cross = keys(w), is_cross(w)
+    q, k, v = make_inputs(w, rank)
     tq, tk, tv = to_dev(q, dev), to_dev(k, dev), to_dev(v, dev)
     o = torch.empty_like(tq)
-    ws = fsa.new_workspace(B, H, S, D, device=dev)
+    ws = (fsa.new_cross_workspace(B, H, S, Sk, D, device=dev) if cross
+          else fsa.new_workspace(B, H, S, D, device=dev))
     stream = torch.cuda.current_stream(dev)
     F = flops(w)
+    if args.schedule and cross:
+        raise SystemExit("--schedule times self-attention workloads only")
     if args.schedule:
         run_schedules(args, w, fsa, tq, tk, tv, o, ws, stream, dev, rank)
         return
@@ -294,10 +323,16 @@ def main():
         for i, fmt in enumerate(FORMATS):
             if ev is not None:
                 ev[i][0].record(stream)
-            fsa.attention_prepare(tq, tk, tv, ws, fmt)
+            if cross:
+                fsa.cross_attention_prepare(tq, tk, tv, ws, fmt)
+            else:
+                fsa.attention_prepare(tq, tk, tv, ws, fmt)
             if ev is not None:
                 ev[i][1].record(stream)
-            fsa.attention_run(ws, o, fmt, THRESHOLD)
+            if cross:
+                fsa.cross_attention_run(ws, o, Sk, fmt, THRESHOLD)
+            else:
+                fsa.attention_run(ws, o, fmt, THRESHOLD)
             if ev is not None:
                 ev[i][2].record(stream)
 
@@ -345,7 +380,7 @@ def main():
             "attention_tflops": F / ka / 1e12,
             "with_quantize_tflops": F / (ka + kq) / 1e12,
             "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
-            "quantize_gbs": (3 * B * H * S * D * (2 + 1 + 1 / 32)) / kq / 1e9,
+            "quantize_gbs": (B * H * (S + 2 * Sk) * D * (2 + 1 + 1 / 32)) / kq / 1e9,
         }
     per_format["mxfp4"]["frac_of_fp4_qk_roofline"] = (
         per_format["mxfp4"]["attention_tflops"] /
@@ -353,7 +388,7 @@ def main():
 
     # in-house BF16 flash-attention baseline, same inputs
     bf16 = None
-    if not args.no_bf16:
+    if not args.no_bf16 and not cross:  # the BF16 kernel is self-attention only
         fsa.bf16_attention_fwd(tq, tk, tv, out=o)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -383,7 +418,10 @@ def main():
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
             for fmt in FORMATS:
-                fsa.attention_fwd(dq, dk, dv, fmt=fmt, threshold=THRESHOLD, out=o)
+                if cross:
+                    fsa.cross_attention_fwd(dq, dk, dv, fmt=fmt, threshold=THRESHOLD, out=o)
+                else:
+                    fsa.attention_fwd(dq, dk, dv, fmt=fmt, threshold=THRESHOLD, out=o)
                 ho.copy_(o, non_blocking=True)
 
         e2e_step()
@@ -403,7 +441,8 @@ def main():
             te = float(tt.item())
         nbytes = tq.numel() * 2
         e2e = {"value": world * F * n_calls / te / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": len(FORMATS) * nbytes}
+               "h2d_bytes_per_step": nbytes + 2 * tk.numel() * 2,
+               "d2h_bytes_per_step": len(FORMATS) * nbytes}
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error during e2e")
 
@@ -415,7 +454,7 @@ def main():
         threads = len(os.sched_getaffinity(0))
         f, t = oracle_sample(q, k, v, w, "mxfp8", args.cpu_rows, threads)
         cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{args.cpu_rows} query rows of head 0 (all {S} keys), MXFP8, "
+               "sample": f"{args.cpu_rows} query rows of head 0 (all {Sk} keys), MXFP8, "
                          f"{t:.1f} s; rows are independent so the rate extrapolates exactly"}
 
     a8 = per_format["mxfp8"]
@@ -426,7 +465,8 @@ def main():
                           "(nominal fp8/bf16 ratio); burst-based peak "
                           f"{pk['mx8_burst']:.1f}"),
             "algorithmic_flops_per_launch": F,
-            "traffic": traffic_from_profiles()}
+            # DRAM counters exist for the default workload's kernel only
+            "traffic": traffic_from_profiles() if args.workload == "video-dit" else None}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
@@ -435,7 +475,8 @@ def main():
         "data": "synthetic N(0,1) bf16, seed = rank",
         "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
                    "threshold": THRESHOLD, "non_causal": True,
-                   "l2": f"inputs {2 * B * H * S * D / 1e6:.0f} MB each, larger than the 129 MB L2",
+                   "l2": (f"inputs {2 * B * H * S * D / 1e6:.0f} MB (Q), "
+                          f"{2 * B * H * Sk * D / 1e6:.0f} MB (K, V) each"),
                    "step": "per format: quantize Q,K,V + fused attention"},
         "per_format": per_format,
         "bf16_baseline": bf16,

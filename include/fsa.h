@@ -149,6 +149,39 @@ FSA_API fsa_status fsa_attention_fwd_ex(const void *q, const void *k, const void
                                 const fsa_options *opt, void *stream);
 
 /*
+ * fsa_cross_attention_fwd -- fsa_attention_fwd_ex with queries and keys of
+ * different lengths (cross-attention shapes): q and o are bf16 device
+ * tensors [B][H][Sq][D], k and v [B][H][Sk][D].  Every query row runs the
+ * same per-row method over the Sk keys in KV tiles of 128 (tile 0 of the keys
+ * freezes the reference, keys >= Sk are masked); rows are independent, so
+ * with Sq = Sk this is exactly fsa_attention_fwd_ex.  The pages measure
+ * self-attention only ("Fused-Softmax shifts ...", paragraph 9: only
+ * self-attention was swapped in the video model); this entry point is the
+ * library's generalisation.  opt->rollback_bits, when given, is
+ * [B*H*Sq][ceil(Sk/128)]; opt->workspace, when given, needs
+ * fsa_cross_attention_workspace_size() bytes.  Requirements as for
+ * fsa_attention_fwd with Sq, Sk >= 1.
+ */
+FSA_API fsa_status fsa_cross_attention_fwd(const void *q, const void *k, const void *v, void *o,
+                                           int B, int H, int Sq, int Sk, int D, int fmt,
+                                           float threshold, const fsa_options *opt, void *stream);
+
+/* Bytes of device workspace fsa_cross_attention_fwd needs (MX copies of Q,
+ * K, V and their scales).  0 for invalid arguments. */
+FSA_API uint64_t fsa_cross_attention_workspace_size(int B, int H, int Sq, int Sk, int D, int fmt);
+
+/* The two halves of fsa_cross_attention_fwd, as fsa_attention_prepare /
+ * fsa_attention_run below with q [B][H][Sq][D] and k, v [B][H][Sk][D]; the
+ * workspace needs fsa_cross_attention_workspace_size() bytes. */
+FSA_API fsa_status fsa_cross_attention_prepare(const void *q, const void *k, const void *v, int B,
+                                               int H, int Sq, int Sk, int D, int fmt,
+                                               void *workspace, uint64_t workspace_bytes,
+                                               void *stream);
+FSA_API fsa_status fsa_cross_attention_run(const void *workspace, uint64_t workspace_bytes, void *o,
+                                           int B, int H, int Sq, int Sk, int D, int fmt,
+                                           float threshold, const fsa_options *opt, void *stream);
+
+/*
  * The two halves of fsa_attention_fwd_ex, for callers that keep the MX
  * copies (e.g. quantize K/V once and attend many times) or time the parts.
  *

@@ -27,7 +27,9 @@ STATUS = {0: "FSA_OK", 1: "FSA_ERR_INVALID_ARGUMENT", 2: "FSA_ERR_UNSUPPORTED",
 # every symbol include/fsa.h declares
 EXPORTS = ("fsa_quantize_mx", "fsa_attention_fwd", "fsa_attention_fwd_ex",
            "fsa_attention_prepare", "fsa_attention_run", "fsa_attention_workspace_size", "fsa_bf16_attention_fwd", "fsa_get_device_error",
-           "fsa_status_string", "fsa_release_workspace", "fsa_attention_fwd_noalloc")
+           "fsa_status_string", "fsa_release_workspace", "fsa_attention_fwd_noalloc",
+           "fsa_cross_attention_fwd", "fsa_cross_attention_workspace_size",
+           "fsa_cross_attention_prepare", "fsa_cross_attention_run")
 
 
 class FsaError(RuntimeError):
@@ -76,6 +78,17 @@ def load(path: str | None = None):
             lib.fsa_attention_run.restype = I
             lib.fsa_attention_workspace_size.argtypes = [I, I, I, I, I]
             lib.fsa_attention_workspace_size.restype = ctypes.c_uint64
+            lib.fsa_cross_attention_fwd.argtypes = [V, V, V, V, I, I, I, I, I, I, F,
+                                                    ctypes.POINTER(Options), V]
+            lib.fsa_cross_attention_fwd.restype = I
+            lib.fsa_cross_attention_workspace_size.argtypes = [I, I, I, I, I, I]
+            lib.fsa_cross_attention_workspace_size.restype = ctypes.c_uint64
+            lib.fsa_cross_attention_prepare.argtypes = [V, V, V, I, I, I, I, I, I, V,
+                                                        ctypes.c_uint64, V]
+            lib.fsa_cross_attention_prepare.restype = I
+            lib.fsa_cross_attention_run.argtypes = [V, ctypes.c_uint64, V, I, I, I, I, I, I, F,
+                                                    ctypes.POINTER(Options), V]
+            lib.fsa_cross_attention_run.restype = I
             lib.fsa_attention_fwd_noalloc.argtypes = [V, V, V, V, I, I, I, I, I, F, V]
             lib.fsa_attention_fwd_noalloc.restype = I
             lib.fsa_bf16_attention_fwd.argtypes = [V, V, V, V, I, I, I, I, V]
@@ -157,6 +170,71 @@ def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=No
                                        FORMATS[fmt], float(threshold), ctypes.byref(opt),
                                        _stream(stream)), "fsa_attention_fwd_ex")
     return o
+
+
+def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
+                        sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
+                        workspace=None, wait_timeout_ms: int = 0, stream=None):
+    """fsa_cross_attention_fwd: q contiguous CUDA bf16 [B, H, Sq, D], k and v
+    [B, H, Sk, D]; returns o [B, H, Sq, D].  rollback_bits: optional uint8
+    CUDA tensor [B*H*Sq, ceil(Sk/128)]."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bhsd(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if k.shape != (B, H, Sk, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Sk, D] with q's B, H and D")
+    o = torch.empty_like(q) if out is None else out
+    opt = Options()
+    opt.sm_scale = sm_scale
+    opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
+    opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    if workspace is not None:
+        opt.workspace = workspace.data_ptr()
+        opt.workspace_bytes = workspace.numel() * workspace.element_size()
+    opt.wait_timeout_ms = wait_timeout_ms
+    _check(load().fsa_cross_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
+                                          FORMATS[fmt], float(threshold), ctypes.byref(opt),
+                                          _stream(stream)), "fsa_cross_attention_fwd")
+    return o
+
+
+def cross_workspace_size(B: int, H: int, Sq: int, Sk: int, D: int, fmt: str = "mxfp8") -> int:
+    return int(load().fsa_cross_attention_workspace_size(B, H, Sq, Sk, D, FORMATS[fmt]))
+
+
+def new_cross_workspace(B: int, H: int, Sq: int, Sk: int, D: int, fmt: str = "mxfp8", device="cuda"):
+    """A device workspace tensor sized for cross_attention_prepare / _run."""
+    return torch.empty(cross_workspace_size(B, H, Sq, Sk, D, fmt), dtype=torch.uint8, device=device)
+
+
+def cross_attention_prepare(q, k, v, workspace, fmt: str = "mxfp8", stream=None):
+    """First half of cross_attention_fwd: MX-quantize q, k, v into `workspace`."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _bhsd(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    _check(load().fsa_cross_attention_prepare(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Sk, D,
+                                              FORMATS[fmt], _ptr(workspace), workspace.numel(),
+                                              _stream(stream)), "fsa_cross_attention_prepare")
+
+
+def cross_attention_run(workspace, out, Sk: int, fmt: str = "mxfp8", threshold: float = 8.0, *,
+                        sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
+                        wait_timeout_ms: int = 0, stream=None):
+    """Second half of cross_attention_fwd: `out` [B, H, Sq, D] fixes B, H, Sq and D;
+    Sk is the key length given to cross_attention_prepare."""
+    _bhsd(out, "out")
+    B, H, Sq, D = out.shape
+    opt = Options()
+    opt.sm_scale = sm_scale
+    opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
+    opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    opt.wait_timeout_ms = wait_timeout_ms
+    _check(load().fsa_cross_attention_run(_ptr(workspace), workspace.numel(), _ptr(out), B, H, Sq,
+                                          Sk, D, FORMATS[fmt], float(threshold), ctypes.byref(opt),
+                                          _stream(stream)), "fsa_cross_attention_run")
+    return out
 
 
 def new_workspace(B: int, H: int, S: int, D: int, fmt: str = "mxfp8", device="cuda"):

@@ -105,7 +105,7 @@ struct Params {
     uint8_t* rollback_bits;
     unsigned long long* rollback_count;
     unsigned int* err_word;
-    int S, D, n_t;
+    int Sq, Sk, D, n_t;  // query rows, keys, head dim, KV tiles ceil(Sk / 128)
     float sm_scale;  // s = sm_scale * accumulator
     float alpha;     // 128 * log2(e) * sm_scale
     float theta;     // gate threshold, natural-log score units
@@ -366,7 +366,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     warp_arrive(&sm.s_free[wg]);
     if (tail) {
         // keys >= S of a partial last tile are masked before the gate and the conversion
-        const int n_valid = p.S - t * kTile;
+        const int n_valid = p.Sk - t * kTile;
         mask32(s0, n_valid);
         mask32(s1, n_valid - 32);
         mask32(s2, n_valid - 64);
@@ -676,11 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = tid & 127;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t s_col = lane_addr + kColS0 + 128 * wg;
-        const bool row_valid = (q0 + r) < p.S;
-        const int64_t grow = static_cast<int64_t>(bh) * p.S + q0 + r;
+        const bool row_valid = (q0 + r) < p.Sq;
+        const int64_t grow = static_cast<int64_t>(bh) * p.Sq + q0 + r;
         RowState rs{0.0f, 0u};
         bool ok = true;
-        const int t_tail = (p.S % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
+        const int t_tail = (p.Sk % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
             ok = softmax_tile<kE4M3>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail, rs);
         if (!ok) raise_abort(sm, p);
@@ -743,9 +743,10 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.rollback_bits = a.rollback_bits;
     p.rollback_count = a.rollback_count;
     p.err_word = a.err_word;
-    p.S = a.S;
+    p.Sq = a.Sq;
+    p.Sk = a.Sk;
     p.D = a.D;
-    p.n_t = (a.S + kTile - 1) / kTile;
+    p.n_t = (a.Sk + kTile - 1) / kTile;
     p.sm_scale = a.sm_scale;
     p.alpha = static_cast<float>(128.0 * 1.4426950408889634 * static_cast<double>(a.sm_scale));
     p.theta = a.threshold;
@@ -766,7 +767,7 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(p.n_t), static_cast<unsigned>(a.BH));
+    dim3 grid(static_cast<unsigned>((a.Sq + kTile - 1) / kTile), static_cast<unsigned>(a.BH));
     kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
     return cudaGetLastError();
 }

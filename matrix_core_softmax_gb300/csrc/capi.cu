@@ -100,12 +100,12 @@ fsa_status current_device(int* dev_out, DeviceState** st_out) {
 }
 
 fsa_status validate_attention(const void* q, const void* k, const void* v, const void* o, int B,
-                              int H, int S, int D) {
+                              int H, int Sq, int Sk, int D) {
     if (!q || !k || !v || !o) return FSA_ERR_INVALID_ARGUMENT;
-    if (B < 1 || H < 1 || S < 1) return FSA_ERR_INVALID_ARGUMENT;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FSA_ERR_INVALID_ARGUMENT;
     if (D != 64 && D != 128) return FSA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(B) * H > 65535) return FSA_ERR_INVALID_ARGUMENT;
-    if (S > (1 << 30)) return FSA_ERR_INVALID_ARGUMENT;
+    if (Sq > (1 << 30) || Sk > (1 << 30)) return FSA_ERR_INVALID_ARGUMENT;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return FSA_ERR_INVALID_ARGUMENT;
     return FSA_OK;
@@ -113,26 +113,27 @@ fsa_status validate_attention(const void* q, const void* k, const void* v, const
 
 }  // namespace
 
-size_t attn_workspace_bytes(int64_t BH, int64_t S, int D) {
-    const int64_t S16 = (S + 15) / 16 * 16;
-    const int64_t nt = (S + kTile - 1) / kTile;
-    return align256(BH * S * D) * 2 + align256(BH * D * S16) +
-           align256(3 * BH * nt * static_cast<int64_t>(kAtomBytes));
+size_t attn_workspace_bytes(int64_t BH, int64_t Sq, int64_t Sk, int D) {
+    const int64_t Sk16 = (Sk + 15) / 16 * 16;
+    const int64_t ntq = (Sq + kTile - 1) / kTile, ntk = (Sk + kTile - 1) / kTile;
+    return align256(BH * Sq * D) + align256(BH * Sk * D) + align256(BH * D * Sk16) +
+           align256((ntq + 2 * ntk) * BH * static_cast<int64_t>(kAtomBytes));
 }
 
-AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t S, int D) {
-    const int64_t S16 = (S + 15) / 16 * 16;
-    const int64_t nt = (S + kTile - 1) / kTile;
+AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t Sq, int64_t Sk, int D) {
+    const int64_t Sk16 = (Sk + 15) / 16 * 16;
+    const int64_t ntq = (Sq + kTile - 1) / kTile, ntk = (Sk + kTile - 1) / kTile;
     uint8_t* p = static_cast<uint8_t*>(base);
     AttnWorkspace w{};
-    w.qc = p; p += align256(BH * S * D);
-    w.kc = p; p += align256(BH * S * D);
-    w.vt = p; p += align256(BH * D * S16);
-    const size_t atoms = static_cast<size_t>(BH * nt) * kAtomBytes;
+    w.qc = p; p += align256(BH * Sq * D);
+    w.kc = p; p += align256(BH * Sk * D);
+    w.vt = p; p += align256(BH * D * Sk16);
+    const size_t atoms_q = static_cast<size_t>(BH * ntq) * kAtomBytes;
+    const size_t atoms_k = static_cast<size_t>(BH * ntk) * kAtomBytes;
     w.qsf = p;
-    w.ksf = p + atoms;
-    w.vsf = p + 2 * atoms;
-    w.sf_bytes_total = 3 * atoms;
+    w.ksf = p + atoms_q;
+    w.vsf = p + atoms_q + atoms_k;
+    w.sf_bytes_total = atoms_q + 2 * atoms_k;
     return w;
 }
 
@@ -149,40 +150,40 @@ fsa_status check_run_args(int fmt, float threshold, const fsa_options& op) {
     return FSA_OK;
 }
 
-fsa_status check_workspace(const void* ws, uint64_t bytes, int64_t BH, int S, int D) {
+fsa_status check_workspace(const void* ws, uint64_t bytes, int64_t BH, int Sq, int Sk, int D) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return FSA_ERR_INVALID_ARGUMENT;
-    if (bytes < attn_workspace_bytes(BH, S, D)) return FSA_ERR_INVALID_ARGUMENT;
+    if (bytes < attn_workspace_bytes(BH, Sq, Sk, D)) return FSA_ERR_INVALID_ARGUMENT;
     return FSA_OK;
 }
 
 // Quantizes Q, K (blocks along D) and V (blocks along keys, transposed).
-fsa_status prepare_impl(const void* q, const void* k, const void* v, int64_t BH, int S, int D,
-                        int fmt, void* ws_base, cudaStream_t st) {
-    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, S, D);
+fsa_status prepare_impl(const void* q, const void* k, const void* v, int64_t BH, int Sq, int Sk,
+                        int D, int fmt, void* ws_base, cudaStream_t st) {
+    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, Sq, Sk, D);
     const int elem = fmt == FSA_MXFP8 ? ELEM_E4M3 : (fmt == FSA_MXFP6 ? ELEM_E2M3 : ELEM_E2M1);
-    const int64_t S16 = (static_cast<int64_t>(S) + 15) / 16 * 16;
+    const int64_t Sk16 = (static_cast<int64_t>(Sk) + 15) / 16 * 16;
     if (cudaMemsetAsync(ws.qsf, 0x7F, ws.sf_bytes_total, st) != cudaSuccess) return FSA_ERR_CUDA;
-    if (launch_quant_rows(static_cast<const uint16_t*>(q), BH * S, D, elem, QL_ATTN, ws.qc, ws.qsf,
-                          S, st) != cudaSuccess ||
-        launch_quant_rows(static_cast<const uint16_t*>(k), BH * S, D, elem, QL_ATTN, ws.kc, ws.ksf,
-                          S, st) != cudaSuccess ||
-        launch_quant_cols(static_cast<const uint16_t*>(v), BH, S, D, elem, QL_ATTN, ws.vt, S16,
+    if (launch_quant_rows(static_cast<const uint16_t*>(q), BH * Sq, D, elem, QL_ATTN, ws.qc, ws.qsf,
+                          Sq, st) != cudaSuccess ||
+        launch_quant_rows(static_cast<const uint16_t*>(k), BH * Sk, D, elem, QL_ATTN, ws.kc, ws.ksf,
+                          Sk, st) != cudaSuccess ||
+        launch_quant_cols(static_cast<const uint16_t*>(v), BH, Sk, D, elem, QL_ATTN, ws.vt, Sk16,
                           ws.vsf, st) != cudaSuccess)
         return FSA_ERR_CUDA;
     return FSA_OK;
 }
 
 // The fused attention kernel on a prepared workspace.
-fsa_status run_impl(void* ws_base, void* o, int64_t BH, int S, int D, int fmt, float threshold,
-                    const fsa_options& op, unsigned int* err, cudaStream_t st) {
-    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, S, D);
-    const int64_t S16 = (static_cast<int64_t>(S) + 15) / 16 * 16;
+fsa_status run_impl(void* ws_base, void* o, int64_t BH, int Sq, int Sk, int D, int fmt,
+                    float threshold, const fsa_options& op, unsigned int* err, cudaStream_t st) {
+    AttnWorkspace ws = attn_workspace_carve(ws_base, BH, Sq, Sk, D);
+    const int64_t Sk16 = (static_cast<int64_t>(Sk) + 15) / 16 * 16;
     CUtensorMap tq, tk, tv;
     const CUtensorMapSwizzle qk_swz =
         D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!make_map_u8(&tq, ws.qc, D, S, BH, D, static_cast<uint64_t>(S) * D, D, kTile, qk_swz) ||
-        !make_map_u8(&tk, ws.kc, D, S, BH, D, static_cast<uint64_t>(S) * D, D, kTile, qk_swz) ||
-        !make_map_u8(&tv, ws.vt, S16, D, BH, S16, static_cast<uint64_t>(S16) * D, kTile, D,
+    if (!make_map_u8(&tq, ws.qc, D, Sq, BH, D, static_cast<uint64_t>(Sq) * D, D, kTile, qk_swz) ||
+        !make_map_u8(&tk, ws.kc, D, Sk, BH, D, static_cast<uint64_t>(Sk) * D, D, kTile, qk_swz) ||
+        !make_map_u8(&tv, ws.vt, Sk16, D, BH, Sk16, static_cast<uint64_t>(Sk16) * D, kTile, D,
                      CU_TENSOR_MAP_SWIZZLE_128B))
         return FSA_ERR_CUDA;
     AttnLaunch a{};
@@ -192,7 +193,8 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int S, int D, int fmt, f
     a.ws = ws;
     a.o = o;
     a.BH = BH;
-    a.S = S;
+    a.Sq = Sq;
+    a.Sk = Sk;
     a.D = D;
     a.fmt = fmt;
     a.sm_scale = op.sm_scale > 0.0f ? op.sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
@@ -205,7 +207,7 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int S, int D, int fmt, f
     a.err_word = err;
     // the kernel writes only the bytes of firings
     if (op.rollback_bits &&
-        cudaMemsetAsync(op.rollback_bits, 0, static_cast<size_t>(BH) * S * ((S + kTile - 1) / kTile), st) !=
+        cudaMemsetAsync(op.rollback_bits, 0, static_cast<size_t>(BH) * Sq * ((Sk + kTile - 1) / kTile), st) !=
             cudaSuccess)
         return FSA_ERR_CUDA;
     return launch_fsa_attention(a, st) == cudaSuccess ? FSA_OK : FSA_ERR_CUDA;
@@ -257,50 +259,74 @@ fsa_status fsa_quantize_mx(const void* x, int64_t batch, int64_t rows, int64_t c
 }
 
 uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fmt) {
-    if (B < 1 || H < 1 || S < 1 || (D != 64 && D != 128) || fmt < 0 || fmt > 2) return 0;
-    return attn_workspace_bytes(static_cast<int64_t>(B) * H, S, D);
+    return fsa_cross_attention_workspace_size(B, H, S, S, D, fmt);
+}
+
+uint64_t fsa_cross_attention_workspace_size(int B, int H, int Sq, int Sk, int D, int fmt) {
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || (D != 64 && D != 128) || fmt < 0 || fmt > 2) return 0;
+    return attn_workspace_bytes(static_cast<int64_t>(B) * H, Sq, Sk, D);
 }
 
 fsa_status fsa_attention_prepare(const void* q, const void* k, const void* v, int B, int H, int S,
                                  int D, int fmt, void* workspace, uint64_t workspace_bytes,
                                  void* stream) {
-    fsa_status s = validate_attention(q, k, v, q, B, H, S, D);
+    return fsa_cross_attention_prepare(q, k, v, B, H, S, S, D, fmt, workspace, workspace_bytes,
+                                       stream);
+}
+
+fsa_status fsa_cross_attention_prepare(const void* q, const void* k, const void* v, int B, int H,
+                                       int Sq, int Sk, int D, int fmt, void* workspace,
+                                       uint64_t workspace_bytes, void* stream) {
+    fsa_status s = validate_attention(q, k, v, q, B, H, Sq, Sk, D);
     if (s != FSA_OK) return s;
     if (fmt < 0 || fmt > 2) return FSA_ERR_INVALID_ARGUMENT;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    s = check_workspace(workspace, workspace_bytes, BH, S, D);
+    s = check_workspace(workspace, workspace_bytes, BH, Sq, Sk, D);
     if (s != FSA_OK) return s;
     int dev;
     DeviceState* ds;
     s = current_device(&dev, &ds);
     if (s != FSA_OK) return s;
-    return prepare_impl(q, k, v, BH, S, D, fmt, workspace, static_cast<cudaStream_t>(stream));
+    return prepare_impl(q, k, v, BH, Sq, Sk, D, fmt, workspace, static_cast<cudaStream_t>(stream));
 }
 
 fsa_status fsa_attention_run(const void* workspace, uint64_t workspace_bytes, void* o, int B,
                              int H, int S, int D, int fmt, float threshold, const fsa_options* opt,
                              void* stream) {
-    fsa_status s = validate_attention(o, o, o, o, B, H, S, D);
+    return fsa_cross_attention_run(workspace, workspace_bytes, o, B, H, S, S, D, fmt, threshold, opt,
+                                   stream);
+}
+
+fsa_status fsa_cross_attention_run(const void* workspace, uint64_t workspace_bytes, void* o, int B,
+                                   int H, int Sq, int Sk, int D, int fmt, float threshold,
+                                   const fsa_options* opt, void* stream) {
+    fsa_status s = validate_attention(o, o, o, o, B, H, Sq, Sk, D);
     if (s != FSA_OK) return s;
     fsa_options defaults{};
     const fsa_options& op = opt ? *opt : defaults;
     s = check_run_args(fmt, threshold, op);
     if (s != FSA_OK) return s;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    s = check_workspace(workspace, workspace_bytes, BH, S, D);
+    s = check_workspace(workspace, workspace_bytes, BH, Sq, Sk, D);
     if (s != FSA_OK) return s;
     int dev;
     DeviceState* ds;
     s = current_device(&dev, &ds);
     if (s != FSA_OK) return s;
-    return run_impl(const_cast<void*>(workspace), o, BH, S, D, fmt, threshold, op, ds->err,
+    return run_impl(const_cast<void*>(workspace), o, BH, Sq, Sk, D, fmt, threshold, op, ds->err,
                     static_cast<cudaStream_t>(stream));
 }
 
 fsa_status fsa_attention_fwd_ex(const void* q, const void* k, const void* v, void* o, int B,
                                 int H, int S, int D, int fmt, float threshold,
                                 const fsa_options* opt, void* stream) {
-    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    return fsa_cross_attention_fwd(q, k, v, o, B, H, S, S, D, fmt, threshold, opt, stream);
+}
+
+fsa_status fsa_cross_attention_fwd(const void* q, const void* k, const void* v, void* o, int B,
+                                   int H, int Sq, int Sk, int D, int fmt, float threshold,
+                                   const fsa_options* opt, void* stream) {
+    fsa_status s = validate_attention(q, k, v, o, B, H, Sq, Sk, D);
     if (s != FSA_OK) return s;
     fsa_options defaults{};
     const fsa_options& op = opt ? *opt : defaults;
@@ -311,14 +337,14 @@ fsa_status fsa_attention_fwd_ex(const void* q, const void* k, const void* v, voi
     s = current_device(&dev, &ds);
     if (s != FSA_OK) return s;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    const size_t need = attn_workspace_bytes(BH, S, D);
+    const size_t need = attn_workspace_bytes(BH, Sq, Sk, D);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (op.workspace) {
-        s = check_workspace(op.workspace, op.workspace_bytes, BH, S, D);
+        s = check_workspace(op.workspace, op.workspace_bytes, BH, Sq, Sk, D);
         if (s != FSA_OK) return s;
-        s = prepare_impl(q, k, v, BH, S, D, fmt, op.workspace, st);
+        s = prepare_impl(q, k, v, BH, Sq, Sk, D, fmt, op.workspace, st);
         if (s != FSA_OK) return s;
-        return run_impl(op.workspace, o, BH, S, D, fmt, threshold, op, ds->err, st);
+        return run_impl(op.workspace, o, BH, Sq, Sk, D, fmt, threshold, op, ds->err, st);
     }
     // library-owned cached workspace, grown on demand; the lock serialises
     // host-side use of it
@@ -336,9 +362,9 @@ fsa_status fsa_attention_fwd_ex(const void* q, const void* k, const void* v, voi
         }
         ds->ws_bytes = need;
     }
-    s = prepare_impl(q, k, v, BH, S, D, fmt, ds->ws, st);
+    s = prepare_impl(q, k, v, BH, Sq, Sk, D, fmt, ds->ws, st);
     if (s != FSA_OK) return s;
-    return run_impl(ds->ws, o, BH, S, D, fmt, threshold, op, ds->err, st);
+    return run_impl(ds->ws, o, BH, Sq, Sk, D, fmt, threshold, op, ds->err, st);
 }
 
 fsa_status fsa_attention_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
@@ -348,7 +374,7 @@ fsa_status fsa_attention_fwd(const void* q, const void* k, const void* v, void* 
 
 fsa_status fsa_bf16_attention_fwd(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int S, int D, void* stream) {
-    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    fsa_status s = validate_attention(q, k, v, o, B, H, S, S, D);
     if (s != FSA_OK) return s;
     int dev;
     DeviceState* ds;
@@ -475,13 +501,13 @@ extern "C" fsa_status fsa_attention_fwd_noalloc(const void* q, const void* k, co
                                                 void* o, int B, int H, int S, int D, int fmt,
                                                 float threshold, void* stream) {
     using namespace fsa;
-    fsa_status s = validate_attention(q, k, v, o, B, H, S, D);
+    fsa_status s = validate_attention(q, k, v, o, B, H, S, S, D);
     if (s != FSA_OK) return s;
     fsa_options defaults{};
     s = check_run_args(fmt, threshold, defaults);
     if (s != FSA_OK) return s;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    if (attn_workspace_bytes(BH, S, D) > kNoAllocBytes) return FSA_ERR_INVALID_ARGUMENT;
+    if (attn_workspace_bytes(BH, S, S, D) > kNoAllocBytes) return FSA_ERR_INVALID_ARGUMENT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FSA_ERR_UNSUPPORTED;
@@ -489,7 +515,7 @@ extern "C" fsa_status fsa_attention_fwd_noalloc(const void* q, const void* k, co
     s = noalloc_setup(dev, &d);
     if (s != FSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = prepare_impl(q, k, v, BH, S, D, fmt, d->ws, st);
+    s = prepare_impl(q, k, v, BH, S, S, D, fmt, d->ws, st);
     if (s != FSA_OK) return s;
-    return run_impl(d->ws, o, BH, S, D, fmt, threshold, defaults, d->status, st);
+    return run_impl(d->ws, o, BH, S, S, D, fmt, threshold, defaults, d->status, st);
 }

@@ -21,18 +21,19 @@ enum QuantLayout : int { QL_PLAIN = 0, QL_ATTN = 1 };
 constexpr int kTile = 128;        // query rows / keys per tile
 constexpr int kAtomBytes = 512;   // scale atom of one 128-row tile
 
-// Workspace of the fused attention call: MX copies of Q, K, V and scales.
+// Workspace of the fused attention call: MX copies of Q, K, V and scales
+// (Sq query rows and Sk keys per head; Sq = Sk for self-attention).
 struct AttnWorkspace {
-    uint8_t* qc;   // [BH][S][D]  E4M3 bit patterns
-    uint8_t* kc;   // [BH][S][D]
-    uint8_t* vt;   // [BH][D][S16] V transposed, keys contiguous, S16 = round_up(S, 16)
-    uint8_t* qsf;  // [BH][n_t][512] atoms, rows = query rows
-    uint8_t* ksf;  // [BH][n_t][512] atoms, rows = keys
-    uint8_t* vsf;  // [BH][n_t][512] atoms, rows = d, blocks along keys
+    uint8_t* qc;   // [BH][Sq][D]  E4M3 bit patterns
+    uint8_t* kc;   // [BH][Sk][D]
+    uint8_t* vt;   // [BH][D][Sk16] V transposed, keys contiguous, Sk16 = round_up(Sk, 16)
+    uint8_t* qsf;  // [BH][ceil(Sq/128)][512] atoms, rows = query rows
+    uint8_t* ksf;  // [BH][ceil(Sk/128)][512] atoms, rows = keys
+    uint8_t* vsf;  // [BH][ceil(Sk/128)][512] atoms, rows = d, blocks along keys
     size_t sf_bytes_total;  // qsf..vsf are contiguous
 };
-size_t attn_workspace_bytes(int64_t BH, int64_t S, int D);
-AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t S, int D);
+size_t attn_workspace_bytes(int64_t BH, int64_t Sq, int64_t Sk, int D);
+AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t Sq, int64_t Sk, int D);
 
 // Quantizer launchers (quantize.cu).
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, int elem,
@@ -50,7 +51,7 @@ struct AttnLaunch {
     AttnWorkspace ws;
     void* o;
     int64_t BH;
-    int S, D, fmt;
+    int Sq, Sk, D, fmt;  // query rows and keys per head
     float sm_scale, threshold;
     uint8_t* rollback_bits;
     unsigned long long* rollback_count;

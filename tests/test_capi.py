@@ -66,6 +66,26 @@ def test_attention_argument_validation(lib):
     assert _attn(lib, B=300, H=300) == 1            # more than 65535 heads
 
 
+def test_cross_attention_workspace_and_validation(lib):
+    # Sq = Sk is the self-attention workspace; each length sizes its own part
+    assert lib.fsa_cross_attention_workspace_size(1, 2, 512, 512, 64, 0) == \
+        lib.fsa_attention_workspace_size(1, 2, 512, 64, 0)
+    small, big = (lib.fsa_cross_attention_workspace_size(1, 2, 100, sk, 128, 1) for sk in (300, 3000))
+    assert big - small >= 2 * 2 * 2700 * 128            # K and V^T copies grow with Sk
+    assert lib.fsa_cross_attention_workspace_size(1, 2, 0, 300, 64, 0) == 0
+    assert lib.fsa_cross_attention_workspace_size(1, 2, 300, 0, 64, 0) == 0
+    P = ctypes.c_void_p
+
+    def cross(q=16, Sq=8, Sk=8, D=64):
+        return lib.fsa_cross_attention_fwd(P(q) if q else None, P(16), P(16), P(16), 1, 1, Sq, Sk, D,
+                                           0, 8.0, None, None)
+    assert cross(q=0) == 1
+    assert cross(Sq=0) == 1
+    assert cross(Sk=0) == 1
+    assert cross(Sk=-3) == 1
+    assert cross(D=96) == 2
+
+
 def test_bf16_attention_argument_validation(lib):
     P = ctypes.c_void_p
     assert lib.fsa_bf16_attention_fwd(None, P(16), P(16), P(16), 1, 1, 8, 64, None) == 1
