@@ -275,7 +275,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=768)
+    ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--schedule", action="store_true",
                     help="time the 20-step hybrid precision schedule against all-BF16 and all-MXFP4")
