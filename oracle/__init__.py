@@ -60,6 +60,7 @@ class _Params(ctypes.Structure):
         ("tile", ctypes.c_int),
         ("threshold", ctypes.c_double),
         ("sm_scale", ctypes.c_double),
+        ("gate_mode", ctypes.c_int),
     ]
 
 
@@ -161,7 +162,7 @@ MODES = ("fused", "conventional", "exact", "exact_frozen", "operands_only")
 def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = "fused",
               threshold: float = 8.0, tile: int = 128, sm_scale: float = 0.0,
               rows=None, threads: int | None = None, want_bits: bool = False,
-              want_margins: bool = False):
+              want_margins: bool = False, gate: str = "fp32"):
     """Oracle attention on bf16 bit patterns q[BH][Sq][D], k/v[BH][Sk][D]
     (uint16; Sq = Sk for self-attention).
 
@@ -176,6 +177,9 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
       "exact_frozen"  -- the method's frozen reference and gate with exact exp
                          and no quantization (equals "exact" for any theta).
     rows: optional global query-row indices bh*Sq+i; outputs follow that order.
+    gate: "fp32" (tile max - m > theta) or "shortcut" (the tile's largest P
+    block scale under the frozen reference exceeds the scale of theta's code;
+    fused mode only).
     Returns a dict with "out" (float64 [n][D]), "out_bf16" (uint16),
     "m", "l", "rollback_count" and optionally "bits" / "margins" [n][n_t].
     """
@@ -193,6 +197,9 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
     qkv_fmt, p_fmt = FORMATS[fmt] if fmt is not None else (-1, -1)
     p = _Params()
     p.tile, p.threshold, p.sm_scale = tile, float(threshold), float(sm_scale)
+    if gate not in ("fp32", "shortcut"):
+        raise ValueError(gate)
+    p.gate_mode = 1 if gate == "shortcut" else 0
     if mode == "fused":
         p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = qkv_fmt, p_fmt, 1, 0, 0
     elif mode == "conventional":

@@ -262,6 +262,11 @@ typedef struct {
     int tile;           /* keys per KV tile (the gate's granularity) */
     double threshold;   /* gate threshold theta; +Inf disables the gate */
     double sm_scale;    /* score scale; <= 0 means 1/sqrt(D) */
+    int gate_mode;      /* 0: the FP32 gate, tile max - m > theta;
+                           1: the shortcut on converted values: the tile's
+                              largest P block scale (frozen reference) exceeds
+                              the scale of a block whose largest weight is the
+                              code of theta (needs p_fmt >= 0, exp_mode 1) */
 } ora_params;
 
 typedef struct {
@@ -284,6 +289,22 @@ typedef struct {
     int64_t count;              /* rollbacks counted by this worker */
     int err;
 } ora_job;
+
+/* The gate shortcut on converted values ("Fused-Softmax shifts ...", para
+ * 12: the fastest four-bit implementation's shortcut can miss a recovery
+ * trigger): with the frozen reference, a tile whose largest score passes it
+ * by d has largest weight code c(d); its largest P block scale is
+ * X(bf16(c(d))).  The shortcut fires when that scale exceeds the scale of a
+ * block whose largest weight is c(theta).  X is a step function, so the
+ * shortcut misses triggers with d just above theta (within theta's scale
+ * binade). */
+static int gate_shortcut_fires(int p_fmt, double d, double theta)
+{
+    const int cd = ora_schraudolph_code(ora_schraudolph_y(d));
+    const int ct = ora_schraudolph_code(ora_schraudolph_y(theta));
+    return ora_mx_scale_exp(p_fmt, ora_bf16_to_double((uint16_t)cd)) >
+           ora_mx_scale_exp(p_fmt, ora_bf16_to_double((uint16_t)ct));
+}
 
 /* One query row: the KV-tile loop of the method, step by step. */
 static int attention_row(ora_job *J, int64_t i, int64_t slot)
@@ -346,8 +367,11 @@ static int attention_row(ora_job *J, int64_t i, int64_t slot)
                 m = tmax;
             } else {
                 double margin = (tmax - m) - P->threshold;
+                int fire = tmax - m > P->threshold;
+                if (P->gate_mode == 1 && P->p_fmt >= 0)
+                    fire = gate_shortcut_fires(P->p_fmt, tmax - m, P->threshold);
                 if (J->margins) J->margins[slot * n_t + t] = margin;
-                if (tmax - m > P->threshold) {
+                if (fire) {
                     double r = exp(m - tmax);
                     for (d = 0; d < D; d++) O[d] *= r;
                     l *= r;
