@@ -61,6 +61,8 @@ class _Params(ctypes.Structure):
         ("threshold", ctypes.c_double),
         ("sm_scale", ctypes.c_double),
         ("gate_mode", ctypes.c_int),
+        ("efq_tau", ctypes.c_double),
+        ("efq_h", ctypes.c_double),
     ]
 
 
@@ -156,13 +158,19 @@ def mx_quantize(x_bits: np.ndarray, block_axis: int, fmt: int):
 
 
 # ------------------------------------------------------------- attention --
-MODES = ("fused", "conventional", "exact", "exact_frozen", "operands_only")
+MODES = ("fused", "conventional", "exact", "exact_frozen", "operands_only", "efq", "online")
+
+
+# EFQ affine rule parameters, calibrated offline by oracle/efq_calibrate.py
+# (tests/golden/efq_calibration.txt)
+EFQ_TAU, EFQ_H = -2.44, 0.61
 
 
 def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = "fused",
               threshold: float = 8.0, tile: int = 128, sm_scale: float = 0.0,
               rows=None, threads: int | None = None, want_bits: bool = False,
-              want_margins: bool = False, gate: str = "fp32"):
+              want_margins: bool = False, gate: str = "fp32", efq_tau: float | None = None,
+              efq_h: float | None = None, p_elem: str | None = None):
     """Oracle attention on bf16 bit patterns q[BH][Sq][D], k/v[BH][Sk][D]
     (uint16; Sq = Sk for self-attention).
 
@@ -176,7 +184,17 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
       "exact"         -- FP64 softmax attention on the bf16 inputs.
       "exact_frozen"  -- the method's frozen reference and gate with exact exp
                          and no quantization (equals "exact" for any theta).
+      "efq"           -- EFQ-Softmax: MX Q/K/V (fmt, normally "mxfp4"), online
+                         attention with the running row max, E2M1 P codes
+                         generated directly from the shifted scores with the
+                         affine rule (efq_tau, efq_h; defaults EFQ_TAU, EFQ_H),
+                         l from the same P.
+      "online"        -- online attention with the running max and exact exp,
+                         no quantization (equals "exact").
     rows: optional global query-row indices bh*Sq+i; outputs follow that order.
+    p_elem: optional P element format overriding the format's own ("e4m3",
+    "e2m3", "e2m1"), e.g. MXFP4 with E2M1 P for the conventional baseline of
+    the EFQ comparison.
     gate: "fp32" (tile max - m > theta) or "shortcut" (the tile's largest P
     block scale under the frozen reference exceeds the scale of theta's code;
     fused mode only).
@@ -200,6 +218,8 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
     if gate not in ("fp32", "shortcut"):
         raise ValueError(gate)
     p.gate_mode = 1 if gate == "shortcut" else 0
+    p.efq_tau = EFQ_TAU if efq_tau is None else float(efq_tau)
+    p.efq_h = EFQ_H if efq_h is None else float(efq_h)
     if mode == "fused":
         p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = qkv_fmt, p_fmt, 1, 0, 0
     elif mode == "conventional":
@@ -210,8 +230,14 @@ def attention(q_bits, k_bits, v_bits, *, fmt: str | None = "mxfp8", mode: str = 
         p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = -1, -1, 0, 1, 1
     elif mode == "exact_frozen":
         p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = -1, -1, 0, 0, 1
+    elif mode == "efq":
+        p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = qkv_fmt, -1, 2, 2, 0
+    elif mode == "online":
+        p.qkv_fmt, p.p_fmt, p.exp_mode, p.max_mode, p.l_from_unquantized = -1, -1, 0, 2, 1
     else:
         raise ValueError(mode)
+    if p_elem is not None:
+        p.p_fmt = {"e4m3": 0, "e2m3": 1, "e2m1": 2}[p_elem]
     if rows is None:
         rows_arr = None
         n = BH * Sq

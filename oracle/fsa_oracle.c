@@ -255,9 +255,12 @@ int ora_schraudolph_code(double y)
 typedef struct {
     int qkv_fmt;        /* -1: Q/K/V not quantized; else element format */
     int p_fmt;          /* -1: P not quantized; else element format of P */
-    int exp_mode;       /* 0: exact exp;  1: Schraudolph bf16 code */
+    int exp_mode;       /* 0: exact exp;  1: Schraudolph bf16 code;
+                           2: EFQ-Softmax E2M1 codes (P quantization built in) */
     int max_mode;       /* 0: frozen reference (tile 0) + rollback gate;
-                           1: exact row max over all keys (conventional) */
+                           1: exact row max over all keys (conventional);
+                           2: running row max, O and l rescaled when it grows
+                              (online attention) */
     int l_from_unquantized; /* 1: l sums the unquantized P (conventional) */
     int tile;           /* keys per KV tile (the gate's granularity) */
     double threshold;   /* gate threshold theta; +Inf disables the gate */
@@ -267,6 +270,7 @@ typedef struct {
                               largest P block scale (frozen reference) exceeds
                               the scale of a block whose largest weight is the
                               code of theta (needs p_fmt >= 0, exp_mode 1) */
+    double efq_tau, efq_h;  /* EFQ affine rule: code = clip(floor((r - tau) / h), 0, 7) */
 } ora_params;
 
 typedef struct {
@@ -304,6 +308,40 @@ static int gate_shortcut_fires(int p_fmt, double d, double theta)
     const int ct = ora_schraudolph_code(ora_schraudolph_y(theta));
     return ora_mx_scale_exp(p_fmt, ora_bf16_to_double((uint16_t)cd)) >
            ora_mx_scale_exp(p_fmt, ora_bf16_to_double((uint16_t)ct));
+}
+
+/* EFQ-Softmax probability codes for one block of n <= 32 keys ("EFQ-Softmax:
+ * Exp-Free Quantization for Softmax", sections "B. Block-Scaled E2M1
+ * Probability Representation" and "C. EFQ-Softmax Probability Code
+ * Generation"): from the shifted scores z_j = s_j - m (m the running row
+ * maximum, masked keys excluded) take u_j = z_j log2(e); the block's
+ * exponent-only scale is 2^X with X the smallest integer such that the block's
+ * largest probability 2^(max u) <= 6 * 2^X (6 = the largest E2M1 value),
+ * clamped to [-127, 127]; the residual r_j = u_j - X is mapped to an E2M1
+ * code by uniformly spaced thresholds, code = clip(floor((r - tau) / h), 0,
+ * 7); the quantized probability is that code's E2M1 value times 2^X. */
+static void efq_block(const double *z, int n, double tau, double h, double *pq)
+{
+    double umax = -INFINITY, u[32];
+    int j, X;
+    for (j = 0; j < n; j++) {
+        u[j] = z[j] * M_LOG2E;
+        if (u[j] > umax) umax = u[j];
+    }
+    if (umax == -INFINITY) {            /* every key of the block masked */
+        for (j = 0; j < n; j++) pq[j] = 0.0;
+        return;
+    }
+    X = (int)ceil(umax - log2(6.0));
+    while (exp2(umax) > ldexp(6.0, X)) X++;
+    while (exp2(umax) <= ldexp(6.0, X - 1)) X--;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    for (j = 0; j < n; j++) {
+        double k = floor((u[j] - X - tau) / h);
+        int code = k < 0.0 ? 0 : (k > 7.0 ? 7 : (int)k);
+        pq[j] = ldexp(ora_decode_elem(2, code), X);
+    }
 }
 
 /* One query row: the KV-tile loop of the method, step by step. */
@@ -380,10 +418,29 @@ static int attention_row(ora_job *J, int64_t i, int64_t slot)
                     if (J->bits) J->bits[slot * n_t + t] = 1;
                 }
             }
+        } else if (P->max_mode == 2) {
+            /* online attention: the running maximum, exact rescale on growth */
+            if (t == 0) {
+                m = tmax;
+            } else if (tmax > m) {
+                double r = exp(m - tmax);
+                for (d = 0; d < D; d++) O[d] *= r;
+                l *= r;
+                m = tmax;
+            }
         }
 
         /* Step 4: weights of this tile. */
-        for (j = 0; j < n; j++) {
+        if (P->exp_mode == 2) {
+            /* EFQ: the quantized probabilities come directly from the shifted
+             * scores, block by block (blocks aligned to the absolute key) */
+            int64_t b0;
+            for (j = 0; j < n; j++) pv[j] = s[j] - m;
+            for (b0 = 0; b0 < n; b0 += 32)
+                efq_block(pv + b0, n - b0 < 32 ? (int)(n - b0) : 32, P->efq_tau, P->efq_h, pq + b0);
+            for (j = 0; j < n; j++) pv[j] = pq[j];
+        }
+        for (j = 0; j < n && P->exp_mode != 2; j++) {
             if (P->exp_mode == 0) {
                 pv[j] = exp(s[j] - m);
             } else {
@@ -395,8 +452,9 @@ static int attention_row(ora_job *J, int64_t i, int64_t slot)
 
         /* Step 5: second stage -- the bf16 weights are MX-quantized along the
          * keys in blocks of 32 aligned to the absolute key index. */
-        for (j = 0; j < n; j++) pq[j] = pv[j];
-        if (P->p_fmt >= 0) {
+        if (P->exp_mode != 2)
+            for (j = 0; j < n; j++) pq[j] = pv[j];
+        if (P->p_fmt >= 0 && P->exp_mode != 2) {
             int64_t b0;
             for (b0 = 0; b0 < n; b0 += 32)
                 mx_block(P->p_fmt, pv + b0, n - b0 < 32 ? (int)(n - b0) : 32, NULL, pq + b0);
@@ -478,6 +536,7 @@ int ora_attention_qk(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     int err = ORA_OK;
     int64_t *hrows = NULL, *hslot = NULL;
     double *kd = NULL, *vd = NULL;
+    if (p && p->exp_mode == 2 && (!(p->efq_h > 0.0) || p->tile % 32 != 0)) return ORA_ERR_ARG;
     if (!q || !k || !v || !p || BH < 0 || Sq < 1 || Sk < 1 || D < 1 || D > 256 || p->tile < 1 ||
         (p->qkv_fmt < -1 || p->qkv_fmt > 2) || (p->p_fmt < -1 || p->p_fmt > 2))
         return ORA_ERR_ARG;
