@@ -275,6 +275,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-efq", action="store_true", help="skip the EFQ-Softmax format")
     ap.add_argument("--cpu-rows", type=int, default=6144)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--schedule", action="store_true",
@@ -382,6 +383,35 @@ def main():
             "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
             "quantize_gbs": (B * H * (S + 2 * Sk) * D * (2 + 1 + 1 / 32)) / kq / 1e9,
         }
+    # the EFQ-Softmax producer (MXFP4 Q/K/V, E2M1 P from the shifted scores,
+    # running maximum): timed on its own, not part of the headline value
+    efq = None
+    if not args.no_efq:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t_q, t_a = [], []
+        for s_i in range(max(1, args.warmup) + args.steps):
+            ev[0].record(stream)
+            if cross:
+                fsa.cross_attention_prepare(tq, tk, tv, ws, "mxfp4_efq")
+            else:
+                fsa.attention_prepare(tq, tk, tv, ws, "mxfp4_efq")
+            ev[1].record(stream)
+            if cross:
+                fsa.cross_attention_run(ws, o, Sk, "mxfp4_efq")
+            else:
+                fsa.attention_run(ws, o, "mxfp4_efq")
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if s_i >= max(1, args.warmup):
+                t_q.append(ev[0].elapsed_time(ev[1]) / 1e3)
+                t_a.append(ev[1].elapsed_time(ev[2]) / 1e3)
+        ka = statistics.mean(t_a)
+        efq = {"attention_kernel_ms": 1e3 * ka, "quantize_ms": 1e3 * statistics.mean(t_q),
+               "attention_tflops": F / ka / 1e12, "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
+               "note": "EFQ-Softmax producer: MXFP4 Q/K/V, running row maximum, E2M1 P"}
+        if fsa.get_device_error() != 0:
+            raise RuntimeError("device error in the EFQ format")
+
     per_format["mxfp4"]["frac_of_fp4_qk_roofline"] = (
         per_format["mxfp4"]["attention_tflops"] /
         (2.0 / (1.0 / pk["fp4_sustained"] + 1.0 / pk["mx8_sustained"])))
@@ -480,6 +510,7 @@ def main():
                    "step": "per format: quantize Q,K,V + fused attention"},
         "per_format": per_format,
         "bf16_baseline": bf16,
+        "efq_format": efq,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,

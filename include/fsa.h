@@ -48,7 +48,20 @@ extern "C" {
 /* Attention formats ("Fused-Softmax shifts ...", paragraph 8): element type
  * of Q/K/V and of P.  MXFP8: E4M3 / E4M3.  MXFP6: E2M3 / E2M3.
  * MXFP4: E2M1 / E2M3 (the MXFP4 variant keeps six-bit P). */
-typedef enum { FSA_MXFP8 = 0, FSA_MXFP6 = 1, FSA_MXFP4 = 2 } fsa_format;
+typedef enum {
+    FSA_MXFP8 = 0,     /* E4M3 Q/K/V, E4M3 P */
+    FSA_MXFP6 = 1,     /* E2M3 Q/K/V, E2M3 P */
+    FSA_MXFP4 = 2,     /* E2M1 Q/K/V, six-bit E2M3 P */
+    /* E2M1 Q/K/V with the EFQ-Softmax P producer ("EFQ-Softmax: Exp-Free
+     * Quantization for Softmax", sections B-C and "A. Integration with Online
+     * Attention"): online attention with the running row maximum (O and l
+     * rescaled exactly when it grows; no rollback gate, `threshold` is
+     * ignored and no firings are reported) and E2M1 P generated directly
+     * from the shifted scores: per 32-key block, u = (s - m) log2(e), scale
+     * 2^X with X = ceil(max u - log2 6), code = clip(floor((u - X - tau) /
+     * h), 0, 7); the same P feeds O and l.  tau, h: fsa_options. */
+    FSA_MXFP4_EFQ = 3
+} fsa_format;
 
 /* Element types of fsa_quantize_mx. */
 typedef enum { FSA_ELEM_E4M3 = 0, FSA_ELEM_E2M3 = 1, FSA_ELEM_E2M1 = 2 } fsa_elem;
@@ -89,6 +102,10 @@ typedef struct {
     /* Bounded-wait limit of the kernels in milliseconds; <= 0 means 2000. */
     int wait_timeout_ms;
     int debug_flags;
+    /* FSA_MXFP4_EFQ's affine rule; efq_h <= 0 selects the library's offline
+     * calibration, tau = -2.44, h = 0.61 (the pages print no values). */
+    float efq_tau;
+    float efq_h;
 } fsa_options;
 
 /*

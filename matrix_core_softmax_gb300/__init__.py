@@ -16,8 +16,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfsa.so")
 
-FSA_MXFP8, FSA_MXFP6, FSA_MXFP4 = 0, 1, 2
-FORMATS = {"mxfp8": FSA_MXFP8, "mxfp6": FSA_MXFP6, "mxfp4": FSA_MXFP4}
+FSA_MXFP8, FSA_MXFP6, FSA_MXFP4, FSA_MXFP4_EFQ = 0, 1, 2, 3
+FORMATS = {"mxfp8": FSA_MXFP8, "mxfp6": FSA_MXFP6, "mxfp4": FSA_MXFP4, "mxfp4_efq": FSA_MXFP4_EFQ}
 ELEM_E4M3, ELEM_E2M3, ELEM_E2M1 = 0, 1, 2
 DEBUG_SKIP_KV_ARRIVE = 0x1
 
@@ -47,6 +47,8 @@ class Options(ctypes.Structure):
         ("workspace_bytes", ctypes.c_uint64),
         ("wait_timeout_ms", ctypes.c_int),
         ("debug_flags", ctypes.c_int),
+        ("efq_tau", ctypes.c_float),
+        ("efq_h", ctypes.c_float),
     ]
 
 
@@ -147,7 +149,7 @@ def workspace_size(B: int, H: int, S: int, D: int, fmt: str = "mxfp8") -> int:
 
 def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                   sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                  workspace=None, wait_timeout_ms: int = 0, debug_flags: int = 0, stream=None):
+                  workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, debug_flags: int = 0, stream=None):
     """Fused-Softmax MX attention forward (fsa_attention_fwd_ex).
 
     q, k, v: contiguous CUDA bf16 [B, H, S, D].  rollback_bits: optional uint8
@@ -164,6 +166,7 @@ def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=No
     if workspace is not None:
         opt.workspace = workspace.data_ptr()
         opt.workspace_bytes = workspace.numel() * workspace.element_size()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
     opt.wait_timeout_ms = wait_timeout_ms
     opt.debug_flags = debug_flags
     _check(load().fsa_attention_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
@@ -174,7 +177,7 @@ def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=No
 
 def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                         sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                        workspace=None, wait_timeout_ms: int = 0, stream=None):
+                        workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
     """fsa_cross_attention_fwd: q contiguous CUDA bf16 [B, H, Sq, D], k and v
     [B, H, Sk, D]; returns o [B, H, Sq, D].  rollback_bits: optional uint8
     CUDA tensor [B*H*Sq, ceil(Sk/128)]."""
@@ -192,6 +195,7 @@ def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, 
     if workspace is not None:
         opt.workspace = workspace.data_ptr()
         opt.workspace_bytes = workspace.numel() * workspace.element_size()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_cross_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
                                           FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -221,7 +225,7 @@ def cross_attention_prepare(q, k, v, workspace, fmt: str = "mxfp8", stream=None)
 
 def cross_attention_run(workspace, out, Sk: int, fmt: str = "mxfp8", threshold: float = 8.0, *,
                         sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                        wait_timeout_ms: int = 0, stream=None):
+                        wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
     """Second half of cross_attention_fwd: `out` [B, H, Sq, D] fixes B, H, Sq and D;
     Sk is the key length given to cross_attention_prepare."""
     _bhsd(out, "out")
@@ -230,6 +234,7 @@ def cross_attention_run(workspace, out, Sk: int, fmt: str = "mxfp8", threshold: 
     opt.sm_scale = sm_scale
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_cross_attention_run(_ptr(workspace), workspace.numel(), _ptr(out), B, H, Sq,
                                           Sk, D, FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -254,7 +259,7 @@ def attention_prepare(q, k, v, workspace, fmt: str = "mxfp8", stream=None):
 
 def attention_run(workspace, out, fmt: str = "mxfp8", threshold: float = 8.0, *,
                   sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                  wait_timeout_ms: int = 0, stream=None):
+                  wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
     """Second half of attention_fwd: the fused kernel on a prepared workspace;
     `out` is the bf16 [B, H, S, D] output and fixes the shape."""
     _bhsd(out, "out")
@@ -263,6 +268,7 @@ def attention_run(workspace, out, fmt: str = "mxfp8", threshold: float = 8.0, *,
     opt.sm_scale = sm_scale
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_attention_run(_ptr(workspace), workspace.numel(), _ptr(out), B, H, S, D,
                                     FORMATS[fmt], float(threshold), ctypes.byref(opt),

@@ -116,7 +116,16 @@ struct Params {
     // integer multiply-add runs on the FMA pipe, while a constant multiplier
     // would become a shift on the integer ALU, the softmax warps' busiest pipe
     uint32_t mul8, mul16;
+    uint32_t mul4;  // 2^4, the same for the EFQ code nibbles
+    // EFQ producer: c = sm_scale * log2(e); code = clip(floor((r - tau) / h), 0, 7)
+    float efq_c, efq_a8, efq_inv8h, efq_tau;  // a8 = c / (8 h), inv8h = 1 / (8 h)
 };
+
+// P producer of a kernel instance: the method's Schraudolph code and
+// two-stage conversion to E4M3 (MXFP8) or six-bit E2M3 (MXFP6, MXFP4) with
+// the frozen reference and rollback gate, or the EFQ-Softmax E2M1 producer
+// with the running row maximum.
+enum PProducer : int { kPE4M3 = 0, kPE2M3 = 1, kPEfq = 2 };
 
 __device__ __forceinline__ void raise_abort(Smem& sm, const Params& p) {
     sm.abort = 1;
@@ -149,6 +158,17 @@ __device__ __forceinline__ void maxmin32(const uint32_t (&v)[32], float& mx, flo
     const float b0 = fmin3(b[0], b[1], b[2]), b1 = fmin3(b[3], b[4], b[5]), b2 = fmin3(b[6], b[7], b[8]);
     mx = fmax3(fmax3(a0, a1, a2), a[9], a[10]);
     mn = fmin3(fmin3(b0, b1, b2), b[9], b[10]);
+}
+
+// Maximum of 32 raw scores (three-input max in a depth-4 tree).
+__device__ __forceinline__ float max32(const uint32_t (&v)[32]) {
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i)
+        a[i] = fmax3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
+    a[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+    return fmax3(fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmax3(a[6], a[7], a[8])), a[9],
+                 a[10]);
 }
 
 // Keys at or beyond n_valid (relative to this 32-key chunk) become -inf.
@@ -276,6 +296,53 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xFFFFFFFFu, w);
 }
 
+// a * b + c saturated to [0, 1] (a NaN or -inf operand gives 0)
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+    float d;
+    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// EFQ-Softmax codes of one 32-key block ("EFQ-Softmax: Exp-Free Quantization
+// for Softmax", sections "B. Block-Scaled E2M1 Probability Representation"
+// and "C. EFQ-Softmax Probability Code Generation"): with u = (s - m) c the
+// shifted score in log2 units, the exponent-only scale 2^X has X = ceil(max u
+// - log2 6) (the smallest X with 2^(max u) <= 6 * 2^X, 6 the largest E2M1
+// value), and each residual r = u - X gives code = clip(floor((r - tau) /
+// h), 0, 7).  Done as v / 8 = s * c / (8 h) + b8 saturated to [0, 1], then
+// floor(8 (1 - 2^-24) v / 8) by a round-down add of 1.5 * 2^23, so that the
+// low bits of the sum are the code (7 when saturated).  Four codes form a
+// byte-permute selector (three integer multiply-adds) that looks the E4M3
+// patterns of the E2M1 values up in two registers.  Returns X + 127.
+__device__ __forceinline__ uint32_t efq_block(const uint32_t (&v)[32], float bmax, float m_acc,
+                                              const Params& p, uint32_t (&w)[8]) {
+    constexpr float kLog2Six = 2.5849625007211563f;
+    const float xf = fminf(fmaxf(ceilf(__fmaf_rn(bmax - m_acc, p.efq_c, -kLog2Six)), -127.0f), 127.0f);
+    const float b8 = __fmaf_rn(-m_acc, p.efq_a8, -(xf + p.efq_tau) * p.efq_inv8h);
+    const float2 k2 = make_float2(7.99999952316284f, 7.99999952316284f);  // 8 - 2^-21
+    const float2 m2 = make_float2(kMagic, kMagic);
+    constexpr uint32_t kTabLo = 0x3C383000u, kTabHi = 0x4C484440u;  // E4M3 of 0, .5, 1, 1.5 | 2, 3, 4, 6
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float2 x0, x1;
+        x0.x = fma_sat(__uint_as_float(v[4 * i]), p.efq_a8, b8);
+        x0.y = fma_sat(__uint_as_float(v[4 * i + 1]), p.efq_a8, b8);
+        x1.x = fma_sat(__uint_as_float(v[4 * i + 2]), p.efq_a8, b8);
+        x1.y = fma_sat(__uint_as_float(v[4 * i + 3]), p.efq_a8, b8);
+        asm("fma.rm.f32x2 %0, %0, %1, %2;" : "+l"(*reinterpret_cast<unsigned long long*>(&x0))
+            : "l"(*reinterpret_cast<const unsigned long long*>(&k2)),
+              "l"(*reinterpret_cast<const unsigned long long*>(&m2)));
+        asm("fma.rm.f32x2 %0, %0, %1, %2;" : "+l"(*reinterpret_cast<unsigned long long*>(&x1))
+            : "l"(*reinterpret_cast<const unsigned long long*>(&k2)),
+              "l"(*reinterpret_cast<const unsigned long long*>(&m2)));
+        // low 16 bits: code0 | code1 << 4 | code2 << 8 | code3 << 12
+        const uint32_t lo = __float_as_uint(x0.y) * p.mul4 + __float_as_uint(x0.x);
+        const uint32_t hi = __float_as_uint(x1.y) * p.mul4 + __float_as_uint(x1.x);
+        w[i] = __byte_perm(kTabLo, kTabHi, hi * p.mul8 + lo);
+    }
+    return static_cast<uint32_t>(static_cast<int>(xf) + 127);
+}
+
 // The two-stage conversion of a whole tile for row r (four 32-key blocks):
 // block scales from the block maxima, then the E4M3 patterns of the row in
 // w0..w3 (keys 32 b .. 32 b + 31 in w_b).  Returns the four E8M0 scale bytes
@@ -327,6 +394,26 @@ struct RowState {
     unsigned fired;       // gate firings of this row
 };
 
+// O and l of this thread's row scaled by `rescale` in TMEM (the previous
+// tile's PV product has retired).
+__device__ __forceinline__ void rescale_o(uint32_t lane_addr, int D, float rescale) {
+    tc_fence_after();
+    uint32_t rr[32];
+    for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(lane_addr + kColO + 32 * c, rr);
+        tmem_ld_wait();
+        tmem_reg_dep(rr);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * rescale);
+        tmem_st32(lane_addr + kColO + 32 * c, rr);
+    }
+    uint32_t lv;
+    tmem_ld1(lane_addr + kColO + D, lv);
+    tmem_ld_wait();
+    tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
+    tmem_st_wait();
+}
+
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
@@ -334,7 +421,7 @@ struct RowState {
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
-template <bool kE4M3>
+template <int kP>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
                                              bool row_valid, int64_t grow, bool tail, RowState& rs) {
@@ -372,70 +459,88 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         mask32(s2, n_valid - 64);
         mask32(s3, n_valid - 96);
     }
-    float bmax[4], bmin[4];
-    maxmin32(s0, bmax[0], bmin[0]);
-    maxmin32(s1, bmax[1], bmin[1]);
-    maxmin32(s2, bmax[2], bmin[2]);
-    maxmin32(s3, bmax[3], bmin[3]);
-    const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
-    // publish this tile's row maximum for the other warpgroup in slot t % 8;
-    // the reader consumes it during its tile t + 1, long before this
-    // warpgroup rewrites the slot at tile t + 8 (which needs the reader's
-    // tile t + 7 maximum)
-    sm.tmax_x[t & 7][r] = tmax;
-    warp_arrive(&sm.m_ready[t & 7]);
-    // frozen reference: replay the gate over the previous tile's maximum,
-    // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
-    if (t > 0) {
-        if (!have_prev) {
-            ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
-            prev = sm.tmax_x[ms][r];
-        }
-        if (t == 1 || prev - rs.m_acc > p.theta_raw) rs.m_acc = prev;
-    }
-    bool fire = false;
-    float rescale = 1.0f;
-    if (t == 0) {
-        rs.m_acc = tmax;
-    } else if (tmax - rs.m_acc > p.theta_raw) {
-        fire = true;
-        rescale = expf((rs.m_acc - tmax) * p.sm_scale);
-        rs.m_acc = tmax;
-    }
-    // P buffer pb is free once PV of tile t - 2 retired.  Waited first: PV
-    // products retire in order, so afterwards the barrier of tile t - 1's
-    // buffer is past PV_{t-3} and can only be in the phase of PV_{t-1}
-    // itself (PV_{t+1} needs this tile's P).
-    if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
-    if (__any_sync(0xFFFFFFFFu, fire)) {
-        // the bitmap was zeroed before the launch: only firings are written
-        if (fire && row_valid) {
-            if (p.rollback_bits) p.rollback_bits[grow * p.n_t + t] = 1;
-            ++rs.fired;
-        }
-        // recovery: once PV of the previous tile retired, O and l of the
-        // firing rows are scaled by exp(m_old - m_new) in TMEM
-        ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
-        tc_fence_after();
-        uint32_t rr[32];
-        for (int c = 0; c < D / 32; ++c) {
-            tmem_ld32(lane_addr + kColO + 32 * c, rr);
-            tmem_ld_wait();
-            tmem_reg_dep(rr);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) rr[j] = __float_as_uint(__uint_as_float(rr[j]) * rescale);
-            tmem_st32(lane_addr + kColO + 32 * c, rr);
-        }
-        uint32_t lv;
-        tmem_ld1(lane_addr + kColO + D, lv);
-        tmem_ld_wait();
-        tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
-        tmem_st_wait();
-    }
     uint32_t w0[8], w1[8], w2[8], w3[8];
-    const uint32_t sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha,
-                                             16249.0f - p.alpha * rs.m_acc, p.mul8, p.mul16,
-                                             w0, w1, w2, w3);
+    uint32_t sfw;
+    if constexpr (kP == kPEfq) {
+        // online attention ("EFQ-Softmax ...", section "A. Integration with
+        // Online Attention"): the running row maximum, replayed over the
+        // other warpgroup's maximum of tile t - 1, and O, l rescaled exactly
+        // when it grows
+        const float bm0 = max32(s0), bm1 = max32(s1), bm2 = max32(s2), bm3 = max32(s3);
+        const float tmax = fmaxf(fmaxf(bm0, bm1), fmaxf(bm2, bm3));
+        sm.tmax_x[t & 7][r] = tmax;
+        warp_arrive(&sm.m_ready[t & 7]);
+        if (t > 0) {
+            if (!have_prev) {
+                ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
+                prev = sm.tmax_x[ms][r];
+            }
+            rs.m_acc = (t == 1) ? prev : fmaxf(rs.m_acc, prev);
+        }
+        const bool grew = t > 0 && tmax > rs.m_acc;
+        const float rescale = grew ? expf((rs.m_acc - tmax) * p.sm_scale) : 1.0f;
+        rs.m_acc = (t == 0) ? tmax : fmaxf(rs.m_acc, tmax);
+        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if (__any_sync(0xFFFFFFFFu, grew)) {
+            ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
+            rescale_o(lane_addr, D, rescale);
+        }
+        const uint32_t sb0 = efq_block(s0, bm0, rs.m_acc, p, w0);
+        const uint32_t sb1 = efq_block(s1, bm1, rs.m_acc, p, w1);
+        const uint32_t sb2 = efq_block(s2, bm2, rs.m_acc, p, w2);
+        const uint32_t sb3 = efq_block(s3, bm3, rs.m_acc, p, w3);
+        sfw = (sb0 + sb1 * p.mul8) + (sb2 + sb3 * p.mul8) * p.mul16;
+    } else {
+        constexpr bool kE4M3 = kP == kPE4M3;
+        float bmax[4], bmin[4];
+        maxmin32(s0, bmax[0], bmin[0]);
+        maxmin32(s1, bmax[1], bmin[1]);
+        maxmin32(s2, bmax[2], bmin[2]);
+        maxmin32(s3, bmax[3], bmin[3]);
+        const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
+        // publish this tile's row maximum for the other warpgroup in slot t % 8;
+        // the reader consumes it during its tile t + 1, long before this
+        // warpgroup rewrites the slot at tile t + 8 (which needs the reader's
+        // tile t + 7 maximum)
+        sm.tmax_x[t & 7][r] = tmax;
+        warp_arrive(&sm.m_ready[t & 7]);
+        // frozen reference: replay the gate over the previous tile's maximum,
+        // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
+        if (t > 0) {
+            if (!have_prev) {
+                ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
+                prev = sm.tmax_x[ms][r];
+            }
+            if (t == 1 || prev - rs.m_acc > p.theta_raw) rs.m_acc = prev;
+        }
+        bool fire = false;
+        float rescale = 1.0f;
+        if (t == 0) {
+            rs.m_acc = tmax;
+        } else if (tmax - rs.m_acc > p.theta_raw) {
+            fire = true;
+            rescale = expf((rs.m_acc - tmax) * p.sm_scale);
+            rs.m_acc = tmax;
+        }
+        // P buffer pb is free once PV of tile t - 2 retired.  Waited first: PV
+        // products retire in order, so afterwards the barrier of tile t - 1's
+        // buffer is past PV_{t-3} and can only be in the phase of PV_{t-1}
+        // itself (PV_{t+1} needs this tile's P).
+        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if (__any_sync(0xFFFFFFFFu, fire)) {
+            // the bitmap was zeroed before the launch: only firings are written
+            if (fire && row_valid) {
+                if (p.rollback_bits) p.rollback_bits[grow * p.n_t + t] = 1;
+                ++rs.fired;
+            }
+            // recovery: once PV of the previous tile retired, O and l of the
+            // firing rows are scaled by exp(m_old - m_new) in TMEM
+            ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
+            rescale_o(lane_addr, D, rescale);
+        }
+        sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc,
+                                  p.mul8, p.mul16, w0, w1, w2, w3);
+    }
     // the P row into TMEM (the A operand of the PV product) and its four
     // scale bytes where the product reads the scales of row r: lane r,
     // column r / 32 of the P buffer's 4-column scale atom
@@ -447,7 +552,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <bool kE4M3>
+template <int kP>
 __global__ void __launch_bounds__(kThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -682,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const int t_tail = (p.Sk % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
-            ok = softmax_tile<kE4M3>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail, rs);
+            ok = softmax_tile<kP>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
             ok = wait_warp(&sm.o_full, 0, p, sm);
@@ -755,9 +860,19 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.debug_flags = a.debug_flags;
     p.mul8 = 1u << 8;
     p.mul16 = 1u << 16;
+    p.mul4 = 1u << 4;
+    {
+        const double c = static_cast<double>(a.sm_scale) * 1.4426950408889634;
+        p.efq_c = static_cast<float>(c);
+        p.efq_a8 = static_cast<float>(c / (8.0 * a.efq_h));
+        p.efq_inv8h = static_cast<float>(1.0 / (8.0 * a.efq_h));
+        p.efq_tau = a.efq_tau;
+    }
     const size_t smem = sizeof(Smem);
-    // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4
-    auto kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<true> : fsa_attn_fwd_kernel<false>;
+    // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4, E2M1 codes of
+    // the EFQ producer for MXFP4-EFQ
+    auto kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<kPE4M3>
+                             : (a.fmt == 3 ? fsa_attn_fwd_kernel<kPEfq> : fsa_attn_fwd_kernel<kPE2M3>);
     // the in-kernel register split assumes exactly kLaunchRegs per thread at
     // launch; anything else could make the increase wait forever
     cudaFuncAttributes fa{};

@@ -143,10 +143,12 @@ namespace fsa {
 namespace {
 
 fsa_status check_run_args(int fmt, float threshold, const fsa_options& op) {
-    if (fmt < 0 || fmt > 2) return FSA_ERR_INVALID_ARGUMENT;
+    if (fmt < 0 || fmt > 3) return FSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(threshold) || threshold < 0.0f || threshold > 80.0f)
         return FSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(op.sm_scale)) return FSA_ERR_INVALID_ARGUMENT;
+    if (fmt == FSA_MXFP4_EFQ && (!std::isfinite(op.efq_tau) || !std::isfinite(op.efq_h)))
+        return FSA_ERR_INVALID_ARGUMENT;
     return FSA_OK;
 }
 
@@ -199,6 +201,9 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int Sq, int Sk, int D, i
     a.fmt = fmt;
     a.sm_scale = op.sm_scale > 0.0f ? op.sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
     a.threshold = threshold;
+    // EFQ affine rule: the library's offline calibration unless given
+    a.efq_tau = op.efq_h > 0.0f ? op.efq_tau : -2.44f;
+    a.efq_h = op.efq_h > 0.0f ? op.efq_h : 0.61f;
     a.rollback_bits = op.rollback_bits;
     a.rollback_count = op.rollback_count;
     a.timeout_ns = static_cast<uint64_t>(op.wait_timeout_ms > 0 ? op.wait_timeout_ms : 2000) *
@@ -263,7 +268,7 @@ uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fmt) {
 }
 
 uint64_t fsa_cross_attention_workspace_size(int B, int H, int Sq, int Sk, int D, int fmt) {
-    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || (D != 64 && D != 128) || fmt < 0 || fmt > 2) return 0;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1 || (D != 64 && D != 128) || fmt < 0 || fmt > 3) return 0;
     return attn_workspace_bytes(static_cast<int64_t>(B) * H, Sq, Sk, D);
 }
 
@@ -279,7 +284,7 @@ fsa_status fsa_cross_attention_prepare(const void* q, const void* k, const void*
                                        uint64_t workspace_bytes, void* stream) {
     fsa_status s = validate_attention(q, k, v, q, B, H, Sq, Sk, D);
     if (s != FSA_OK) return s;
-    if (fmt < 0 || fmt > 2) return FSA_ERR_INVALID_ARGUMENT;
+    if (fmt < 0 || fmt > 3) return FSA_ERR_INVALID_ARGUMENT;
     const int64_t BH = static_cast<int64_t>(B) * H;
     s = check_workspace(workspace, workspace_bytes, BH, Sq, Sk, D);
     if (s != FSA_OK) return s;

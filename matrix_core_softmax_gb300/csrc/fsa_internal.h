@@ -53,6 +53,7 @@ struct AttnLaunch {
     int64_t BH;
     int Sq, Sk, D, fmt;  // query rows and keys per head
     float sm_scale, threshold;
+    float efq_tau, efq_h;  // EFQ affine rule (fmt 3)
     uint8_t* rollback_bits;
     unsigned long long* rollback_count;
     uint64_t timeout_ns;

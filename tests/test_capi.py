@@ -59,7 +59,7 @@ def test_attention_argument_validation(lib):
     assert _attn(lib, B=-1) == 1
     assert _attn(lib, D=96) == 2
     assert _attn(lib, q=8) == 1                     # not 16-byte aligned
-    assert _attn(lib, fmt=3) == 1
+    assert _attn(lib, fmt=4) == 1
     assert _attn(lib, theta=float("nan")) == 1
     assert _attn(lib, theta=-1.0) == 1
     assert _attn(lib, theta=81.0) == 1
