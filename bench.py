@@ -276,7 +276,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-efq", action="store_true", help="skip the EFQ-Softmax format")
-    ap.add_argument("--cpu-rows", type=int, default=6144)
+    ap.add_argument("--cpu-rows", type=int, default=12288)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--schedule", action="store_true",
                     help="time the 20-step hybrid precision schedule against all-BF16 and all-MXFP4")
