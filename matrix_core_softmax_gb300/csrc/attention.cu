@@ -274,6 +274,35 @@ __device__ __forceinline__ bool block_is_linear(float bn, int sb, float alpha, f
     return cmin >= kMagicBits + 128 * max(sb - 6, 1);
 }
 
+// Six-bit P when no code of the tile is a bf16 subnormal (< 128) or falls
+// below 128 (X + 1), X = sb - 127 (the scale with its E2M3 offset): then
+// p / 2^X is a normal FP32 whose pattern is (code << 16) - (X << 23), one
+// integer multiply-add, the same value the general path's multiply gives.
+__device__ __forceinline__ bool block_is_scalable(float bn, int sb, float alpha, float beta) {
+    const int cmin = static_cast<int>(__float_as_uint(__fadd_rn(__fmaf_rn(bn, alpha, beta), kMagic)));
+    return cmin >= kMagicBits + 128 * max(sb - 126, 1);
+}
+
+// E2M3-in-E4M3 patterns of 32 scores with the scaling folded into the bf16
+// reinterpretation: pattern(p / 2^X) = (y + kMagic) * 2^16 - X * 2^23 (mod 2^32).
+__device__ __forceinline__ void convert32_scaled(const uint32_t (&v)[32], float alpha, float beta,
+                                                 int sb, uint32_t mul16, uint32_t (&w)[8]) {
+    const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
+    const float2 m2 = make_float2(kMagic, kMagic);
+    const uint32_t neg_x = static_cast<uint32_t>(127 - sb) << 23;  // -X * 2^23
+    uint32_t e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float2 y = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                              a2, b2);
+        y = __fadd2_rn(y, m2);
+        e[i] = cvt_e4m3x2(__uint_as_float(__float_as_uint(y.x) * mul16 + neg_x),
+                          __uint_as_float(__float_as_uint(y.y) * mul16 + neg_x));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = e[2 * i + 1] * mul16 + e[2 * i];
+}
+
 // inv = 2^-X of the general conversion, X = sb - 127
 __device__ __forceinline__ float general_inv(int sb) { return __int_as_float((254 - sb) << 23); }
 
@@ -369,6 +398,14 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
         convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
         convert32_linear(s3, alpha, beta, linear_kx(sb3), linear_kx2(sb3), mul8, mul16, w3);
+    } else if (!kE4M3 && __all_sync(0xFFFFFFFFu,
+                                    block_is_scalable(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                                      max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
+        // six-bit P, the common case: scaling folded into the reinterpretation
+        convert32_scaled(s0, alpha, beta, sb0, mul16, w0);
+        convert32_scaled(s1, alpha, beta, sb1, mul16, w1);
+        convert32_scaled(s2, alpha, beta, sb2, mul16, w2);
+        convert32_scaled(s3, alpha, beta, sb3, mul16, w3);
     } else if (kE4M3 || __any_sync(0xFFFFFFFFu,
                                    __fmaf_rn(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
                                              alpha, beta) < 0.0f)) {
