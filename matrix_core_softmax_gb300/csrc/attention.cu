@@ -469,8 +469,6 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     uint32_t s0[32], s1[32], s2[32], s3[32];
     tmem_ld32(s_col, s0);
     tmem_ld32(s_col + 32, s1);
-    tmem_ld32(s_col + 64, s2);
-    tmem_ld32(s_col + 96, s3);
     // while the scores travel: non-blocking looks at the other warpgroup's
     // maximum of tile t - 1 and at this tile's P buffer (PV of tile t - 2
     // retired); both are normally complete by now
@@ -483,6 +481,13 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tmem_ld_wait();
     tmem_reg_dep(s0);
     tmem_reg_dep(s1);
+    // the second half travels while the first is reduced
+    tmem_ld32(s_col + 64, s2);
+    tmem_ld32(s_col + 96, s3);
+    float h_max0, h_min0, h_max1, h_min1;
+    maxmin32(s0, h_max0, h_min0);
+    maxmin32(s1, h_max1, h_min1);
+    tmem_ld_wait();
     tmem_reg_dep(s2);
     tmem_reg_dep(s3);
     // the whole tile is in registers: the next score product may reuse S
@@ -529,9 +534,11 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         sfw = (sb0 + sb1 * p.mul8) + (sb2 + sb3 * p.mul8) * p.mul16;
     } else {
         constexpr bool kE4M3 = kP == kPE4M3;
-        float bmax[4], bmin[4];
-        maxmin32(s0, bmax[0], bmin[0]);
-        maxmin32(s1, bmax[1], bmin[1]);
+        float bmax[4] = {h_max0, h_max1, 0.0f, 0.0f}, bmin[4] = {h_min0, h_min1, 0.0f, 0.0f};
+        if (tail) {  // the masked keys change the first half's extrema too
+            maxmin32(s0, bmax[0], bmin[0]);
+            maxmin32(s1, bmax[1], bmin[1]);
+        }
         maxmin32(s2, bmax[2], bmin[2]);
         maxmin32(s3, bmax[3], bmin[3]);
         const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
