@@ -484,9 +484,14 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     // the second half travels while the first is reduced
     tmem_ld32(s_col + 64, s2);
     tmem_ld32(s_col + 96, s3);
-    float h_max0, h_min0, h_max1, h_min1;
-    maxmin32(s0, h_max0, h_min0);
-    maxmin32(s1, h_max1, h_min1);
+    float h_max0, h_min0 = 0.0f, h_max1, h_min1 = 0.0f;
+    if constexpr (kP == kPEfq) {  // the EFQ producer needs no minima
+        h_max0 = max32(s0);
+        h_max1 = max32(s1);
+    } else {
+        maxmin32(s0, h_max0, h_min0);
+        maxmin32(s1, h_max1, h_min1);
+    }
     tmem_ld_wait();
     tmem_reg_dep(s2);
     tmem_reg_dep(s3);
@@ -508,7 +513,10 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // Online Attention"): the running row maximum, replayed over the
         // other warpgroup's maximum of tile t - 1, and O, l rescaled exactly
         // when it grows
-        const float bm0 = max32(s0), bm1 = max32(s1), bm2 = max32(s2), bm3 = max32(s3);
+        // the first half's maxima were taken while the second half loaded
+        // (again after the tail mask)
+        const float bm0 = tail ? max32(s0) : h_max0, bm1 = tail ? max32(s1) : h_max1;
+        const float bm2 = max32(s2), bm3 = max32(s3);
         const float tmax = fmaxf(fmaxf(bm0, bm1), fmaxf(bm2, bm3));
         sm.tmax_x[t & 7][r] = tmax;
         warp_arrive(&sm.m_ready[t & 7]);
