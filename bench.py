@@ -180,6 +180,22 @@ def oracle_sample(q, k, v, w, fmt, n_rows, threads):
     return n_rows * 4.0 * keys(w) * w["D"], dt
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's x (the slowest rank sets a replica run's
+    time); x itself when there is a single process."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(world, flops_per_call, n_calls, elapsed_s):
+    """Whole-job throughput of weakly scaled replicas: every rank ran the
+    same n_calls calls of flops_per_call, the slowest in elapsed_s."""
+    return world * flops_per_call * n_calls / elapsed_s / 1e12
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -362,11 +378,9 @@ def main():
         raise RuntimeError(f"device error: {fsa.status_string(st)}")
     elapsed = t_start.elapsed_time(t_end) / 1e3
     if pg:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        elapsed = float(tt.item())
+        elapsed = max_over_ranks(elapsed, pg, dev)
     n_calls = args.steps * len(FORMATS)
-    value = world * F * n_calls / elapsed / 1e12
+    value = aggregate_tflops(world, F, n_calls, elapsed)
     pk = peaks()
 
     per_format = {}
@@ -466,11 +480,9 @@ def main():
         torch.cuda.synchronize(dev)
         te = e0.elapsed_time(e1) / 1e3
         if pg:
-            tt = torch.tensor([te], device=dev, dtype=torch.float64)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            te = float(tt.item())
+            te = max_over_ranks(te, pg, dev)
         nbytes = tq.numel() * 2
-        e2e = {"value": world * F * n_calls / te / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": aggregate_tflops(world, F, n_calls, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": nbytes + 2 * tk.numel() * 2,
                "d2h_bytes_per_step": len(FORMATS) * nbytes}
         if fsa.get_device_error() != 0:
