@@ -190,7 +190,7 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, 
                                           float inv, uint32_t mul16, uint32_t (&w)[8]) {
     const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
     const float2 m2 = make_float2(kMagic, kMagic), i2 = make_float2(inv, inv);
-    uint32_t e[16];
+    float2 q[2];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         float2 y = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
@@ -202,11 +202,9 @@ __device__ __forceinline__ void convert32(const uint32_t (&v)[32], float alpha, 
         y = __fadd2_rn(y, m2);
         const float2 pw = make_float2(__uint_as_float(__float_as_uint(y.x) * mul16),
                                       __uint_as_float(__float_as_uint(y.y) * mul16));
-        const float2 q = __fmul2_rn(pw, i2);
-        e[i] = cvt_e4m3x2(q.x, q.y);
+        q[i & 1] = __fmul2_rn(pw, i2);
+        if (i & 1) w[i >> 1] = cvt_e4m3x4(q[0].x, q[0].y, q[1].x, q[1].y);
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = e[2 * i + 1] * mul16 + e[2 * i];
 }
 
 // E4M3 P when every score of the 32-key block converts to an E4M3 normal
@@ -290,17 +288,17 @@ __device__ __forceinline__ void convert32_scaled(const uint32_t (&v)[32], float 
     const float2 a2 = make_float2(alpha, alpha), b2 = make_float2(beta, beta);
     const float2 m2 = make_float2(kMagic, kMagic);
     const uint32_t neg_x = static_cast<uint32_t>(127 - sb) << 23;  // -X * 2^23
-    uint32_t e[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float2 y = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                              a2, b2);
-        y = __fadd2_rn(y, m2);
-        e[i] = cvt_e4m3x2(__uint_as_float(__float_as_uint(y.x) * mul16 + neg_x),
-                          __uint_as_float(__float_as_uint(y.y) * mul16 + neg_x));
+    for (int i = 0; i < 8; ++i) {
+        float2 y0 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1])), a2, b2);
+        float2 y1 = __ffma2_rn(make_float2(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])), a2, b2);
+        y0 = __fadd2_rn(y0, m2);
+        y1 = __fadd2_rn(y1, m2);
+        w[i] = cvt_e4m3x4(__uint_as_float(__float_as_uint(y0.x) * mul16 + neg_x),
+                          __uint_as_float(__float_as_uint(y0.y) * mul16 + neg_x),
+                          __uint_as_float(__float_as_uint(y1.x) * mul16 + neg_x),
+                          __uint_as_float(__float_as_uint(y1.y) * mul16 + neg_x));
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = e[2 * i + 1] * mul16 + e[2 * i];
 }
 
 // inv = 2^-X of the general conversion, X = sb - 127

@@ -329,6 +329,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Four FP32 values to four E4M3 bytes of one word (a0 in the low byte): the
+// two pair conversions write the halves of the result register directly, so
+// no 16-bit intermediate has to be widened and repacked.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    asm("{\n.reg .b16 lo, hi;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi};\n}"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
 // Two FP32 values to a packed E2M3 pair (6-bit codes in the low bits of each byte).
 __device__ __forceinline__ uint32_t cvt_e2m3x2(float lo, float hi) {
     uint16_t r;
