@@ -101,6 +101,8 @@ struct Params {
     const uint8_t* q_sf;
     const uint8_t* k_sf;
     const uint8_t* v_sf;
+    const float* q_norm;  // six-bit P: [BH][Sq] bounds of |q^_i|
+    const float* k_norm;  // six-bit P: [BH][n_t] per KV tile, bound of max_j |k^_j|
     __nv_bfloat16* o;
     uint8_t* rollback_bits;
     unsigned long long* rollback_count;
@@ -168,6 +170,17 @@ __device__ __forceinline__ float max32(const uint32_t (&v)[32]) {
         a[i] = fmax3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
     a[10] = fmaxf(__uint_as_float(v[30]), __uint_as_float(v[31]));
     return fmax3(fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmax3(a[6], a[7], a[8])), a[9],
+                 a[10]);
+}
+
+// Minimum of 32 raw scores (three-input min in a depth-4 tree).
+__device__ __forceinline__ float min32(const uint32_t (&v)[32]) {
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i)
+        a[i] = fmin3(__uint_as_float(v[3 * i]), __uint_as_float(v[3 * i + 1]), __uint_as_float(v[3 * i + 2]));
+    a[10] = fminf(__uint_as_float(v[30]), __uint_as_float(v[31]));
+    return fmin3(fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fmin3(a[6], a[7], a[8])), a[9],
                  a[10]);
 }
 
@@ -379,8 +392,8 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
                                                  const uint32_t (&s2)[32], const uint32_t (&s3)[32],
                                                  const float (&bmax)[4], const float (&bmin)[4],
                                                  float alpha, float beta, uint32_t mul8, uint32_t mul16,
-                                                 uint32_t (&w0)[8], uint32_t (&w1)[8], uint32_t (&w2)[8],
-                                                 uint32_t (&w3)[8]) {
+                                                 bool bounded, uint32_t (&w0)[8], uint32_t (&w1)[8],
+                                                 uint32_t (&w2)[8], uint32_t (&w3)[8]) {
     const int sb0 = block_scale_byte<kE4M3>(bmax[0], alpha, beta);
     const int sb1 = block_scale_byte<kE4M3>(bmax[1], alpha, beta);
     const int sb2 = block_scale_byte<kE4M3>(bmax[2], alpha, beta);
@@ -396,10 +409,11 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
         convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
         convert32_linear(s3, alpha, beta, linear_kx(sb3), linear_kx2(sb3), mul8, mul16, w3);
-    } else if (!kE4M3 && __all_sync(0xFFFFFFFFu,
-                                    block_is_scalable(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
-                                                      max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
+    } else if (!kE4M3 && (bounded || __all_sync(0xFFFFFFFFu,
+                                                block_is_scalable(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                                                  max(max(sb0, sb1), max(sb2, sb3)), alpha, beta)))) {
         // six-bit P, the common case: scaling folded into the reinterpretation
+        // (bounded: the warp's norm bound already proves the condition)
         convert32_scaled(s0, alpha, beta, sb0, mul16, w0);
         convert32_scaled(s1, alpha, beta, sb1, mul16, w1);
         convert32_scaled(s2, alpha, beta, sb2, mul16, w2);
@@ -421,6 +435,34 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
     // four bytes < 256 into one word
     return (static_cast<uint32_t>(sb0) + static_cast<uint32_t>(sb1) * mul8) +
            (static_cast<uint32_t>(sb2) + static_cast<uint32_t>(sb3) * mul8) * mul16;
+}
+
+// Six-bit P without block minima.  The scaled conversion (convert32_scaled)
+// is exact when every code c of the row's tile satisfies c >= 128 and
+// c >= 128 (X_max + 1), X_max the largest block exponent with its E2M3 offset
+// (block_is_scalable).  From the scale rule, X_max + 1 = max(floor((C - 241)
+// / 128), 0) - 120 for the row's largest code C, so both hold when
+// C - c_min <= 15601 and c_min >= 128.  Every code lies within 0.51 of
+// alpha (acc - m) + 16249 (FP32 rounding of beta and of the FMA, then the
+// rounding to an integer), and by Cauchy-Schwarz every accumulator of row i,
+// the reference m among them (it is one), lies in [-A, A] with
+// A = |q^_i| max_j |k^_j|.  Hence 2 |alpha| A <= 15000 gives C - c_min <=
+// 15001.1 and c_min >= 16249 - 15000.6: the minima need not be taken.  The
+// norm bounds come from the quantizer with a relative slack of 2^-10, and the
+// 4 % margin to 15601 covers the MMA's accumulation error.  A warp takes the
+// shortcut when all 32 of its rows pass (a NaN or infinite bound fails).
+constexpr float kBoundLimit = 15000.0f;
+
+__device__ __forceinline__ bool warp_bounded(const Params& p, int bh, bool row_valid, int64_t grow) {
+    // the head's largest key-row bound: lane l scans tiles l, l + 32, ...;
+    // non-negative floats (and +inf, NaN) compare like their bit patterns
+    const float* kn = p.k_norm + static_cast<int64_t>(bh) * p.n_t;
+    unsigned km = 0;
+    for (int i = threadIdx.x & 31; i < p.n_t; i += 32) km = max(km, __float_as_uint(kn[i]));
+    km = __reduce_max_sync(0xFFFFFFFFu, km);
+    const float qn = row_valid ? p.q_norm[grow] : 0.0f;  // rows past Sq hold zeros
+    const float a = 2.0f * fabsf(p.alpha) * qn * __uint_as_float(km);
+    return __all_sync(0xFFFFFFFFu, a <= kBoundLimit);
 }
 
 // Per-row state of a softmax thread.
@@ -459,7 +501,8 @@ __device__ __forceinline__ void rescale_o(uint32_t lane_addr, int D, float resca
 template <int kP>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
-                                             bool row_valid, int64_t grow, bool tail, RowState& rs) {
+                                             bool row_valid, int64_t grow, bool tail, bool bounded,
+                                             RowState& rs) {
     const int D = p.D;
     const int pb = t & (kPBuf - 1);
     bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
@@ -483,7 +526,9 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tmem_ld32(s_col + 64, s2);
     tmem_ld32(s_col + 96, s3);
     float h_max0, h_min0 = 0.0f, h_max1, h_min1 = 0.0f;
-    if constexpr (kP == kPEfq) {  // the EFQ producer needs no minima
+    // the EFQ producer needs no minima; six-bit P takes them in a second pass
+    // only where its norm bound does not hold
+    if constexpr (kP != kPE4M3) {
         h_max0 = max32(s0);
         h_max1 = max32(s1);
     } else {
@@ -541,12 +586,30 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     } else {
         constexpr bool kE4M3 = kP == kPE4M3;
         float bmax[4] = {h_max0, h_max1, 0.0f, 0.0f}, bmin[4] = {h_min0, h_min1, 0.0f, 0.0f};
-        if (tail) {  // the masked keys change the first half's extrema too
-            maxmin32(s0, bmax[0], bmin[0]);
-            maxmin32(s1, bmax[1], bmin[1]);
+        // a bounded six-bit warp needs only the block maxima, except on the
+        // tail tile, whose masked keys take the general conversion
+        const bool no_min = !kE4M3 && bounded && !tail;
+        if constexpr (kE4M3) {
+            if (tail) {  // the masked keys change the first half's extrema too
+                maxmin32(s0, bmax[0], bmin[0]);
+                maxmin32(s1, bmax[1], bmin[1]);
+            }
+            maxmin32(s2, bmax[2], bmin[2]);
+            maxmin32(s3, bmax[3], bmin[3]);
+        } else {
+            if (tail) {
+                bmax[0] = max32(s0);
+                bmax[1] = max32(s1);
+            }
+            bmax[2] = max32(s2);
+            bmax[3] = max32(s3);
+            if (!no_min) {  // rare: the exact test of the scaled conversion needs the minima
+                bmin[0] = min32(s0);
+                bmin[1] = min32(s1);
+                bmin[2] = min32(s2);
+                bmin[3] = min32(s3);
+            }
         }
-        maxmin32(s2, bmax[2], bmin[2]);
-        maxmin32(s3, bmax[3], bmin[3]);
         const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
         // publish this tile's row maximum for the other warpgroup in slot t % 8;
         // the reader consumes it during its tile t + 1, long before this
@@ -589,7 +652,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             rescale_o(lane_addr, D, rescale);
         }
         sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc,
-                                  p.mul8, p.mul16, w0, w1, w2, w3);
+                                  p.mul8, p.mul16, no_min, w0, w1, w2, w3);
     }
     // the P row into TMEM (the A operand of the PV product) and its four
     // scale bytes where the product reads the scales of row r: lane r,
@@ -836,8 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         RowState rs{0.0f, 0u};
         bool ok = true;
         const int t_tail = (p.Sk % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
+        // six-bit P: a warp whose rows satisfy the norm bound skips the block minima
+        bool bounded = false;
+        if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
-            ok = softmax_tile<kP>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail, rs);
+            ok = softmax_tile<kP>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail,
+                                  bounded, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
             ok = wait_warp(&sm.o_full, 0, p, sm);
@@ -894,6 +961,8 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.q_sf = a.ws.qsf;
     p.k_sf = a.ws.ksf;
     p.v_sf = a.ws.vsf;
+    p.q_norm = a.ws.qnorm;
+    p.k_norm = a.ws.knorm;
     p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
     p.rollback_bits = a.rollback_bits;
     p.rollback_count = a.rollback_count;

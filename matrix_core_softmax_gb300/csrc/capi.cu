@@ -117,7 +117,8 @@ size_t attn_workspace_bytes(int64_t BH, int64_t Sq, int64_t Sk, int D) {
     const int64_t Sk16 = (Sk + 15) / 16 * 16;
     const int64_t ntq = (Sq + kTile - 1) / kTile, ntk = (Sk + kTile - 1) / kTile;
     return align256(BH * Sq * D) + align256(BH * Sk * D) + align256(BH * D * Sk16) +
-           align256((ntq + 2 * ntk) * BH * static_cast<int64_t>(kAtomBytes));
+           align256((ntq + 2 * ntk) * BH * static_cast<int64_t>(kAtomBytes)) +
+           align256(BH * Sq * 4) + align256(BH * ntk * 4);
 }
 
 AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t Sq, int64_t Sk, int D) {
@@ -134,6 +135,9 @@ AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t Sq, int64_t S
     w.ksf = p + atoms_q;
     w.vsf = p + atoms_q + atoms_k;
     w.sf_bytes_total = atoms_q + 2 * atoms_k;
+    p += align256(static_cast<int64_t>(w.sf_bytes_total));
+    w.qnorm = reinterpret_cast<float*>(p); p += align256(BH * Sq * 4);
+    w.knorm = reinterpret_cast<float*>(p);
     return w;
 }
 
@@ -164,11 +168,17 @@ fsa_status prepare_impl(const void* q, const void* k, const void* v, int64_t BH,
     AttnWorkspace ws = attn_workspace_carve(ws_base, BH, Sq, Sk, D);
     const int elem = fmt == FSA_MXFP8 ? ELEM_E4M3 : (fmt == FSA_MXFP6 ? ELEM_E2M3 : ELEM_E2M1);
     const int64_t Sk16 = (static_cast<int64_t>(Sk) + 15) / 16 * 16;
+    // six-bit P: norm bounds of the quantized rows of Q and (per KV tile) of K,
+    // from which the fused kernel proves that no weight of a row can underflow
+    const bool norms = fmt == FSA_MXFP6 || fmt == FSA_MXFP4;
+    const int64_t ntk = (static_cast<int64_t>(Sk) + kTile - 1) / kTile;
     if (cudaMemsetAsync(ws.qsf, 0x7F, ws.sf_bytes_total, st) != cudaSuccess) return FSA_ERR_CUDA;
+    if (norms && cudaMemsetAsync(ws.knorm, 0, static_cast<size_t>(BH * ntk) * 4, st) != cudaSuccess)
+        return FSA_ERR_CUDA;
     if (launch_quant_rows(static_cast<const uint16_t*>(q), BH * Sq, D, elem, QL_ATTN, ws.qc, ws.qsf,
-                          Sq, st) != cudaSuccess ||
+                          Sq, st, ws.qnorm, norms ? NORM_ROW : NORM_NONE) != cudaSuccess ||
         launch_quant_rows(static_cast<const uint16_t*>(k), BH * Sk, D, elem, QL_ATTN, ws.kc, ws.ksf,
-                          Sk, st) != cudaSuccess ||
+                          Sk, st, ws.knorm, norms ? NORM_TILE_MAX : NORM_NONE) != cudaSuccess ||
         launch_quant_cols(static_cast<const uint16_t*>(v), BH, Sk, D, elem, QL_ATTN, ws.vt, Sk16,
                           ws.vsf, st) != cudaSuccess)
         return FSA_ERR_CUDA;

@@ -31,14 +31,21 @@ struct AttnWorkspace {
     uint8_t* ksf;  // [BH][ceil(Sk/128)][512] atoms, rows = keys
     uint8_t* vsf;  // [BH][ceil(Sk/128)][512] atoms, rows = d, blocks along keys
     size_t sf_bytes_total;  // qsf..vsf are contiguous
+    float* qnorm;  // [BH][Sq] upper bound of |q^_i| (six-bit formats)
+    float* knorm;  // [BH][ceil(Sk/128)] per KV tile: max over its keys of an upper bound of |k^_j|
 };
 size_t attn_workspace_bytes(int64_t BH, int64_t Sq, int64_t Sk, int D);
 AttnWorkspace attn_workspace_carve(void* base, int64_t BH, int64_t Sq, int64_t Sk, int D);
 
+// Row-norm output of the row quantizer (ATTN layout only): none, an upper
+// bound of the Euclidean norm of every quantized row, or per 128-row tile the
+// largest of those bounds (atomic maximum into a zeroed array).
+enum NormMode : int { NORM_NONE = 0, NORM_ROW = 1, NORM_TILE_MAX = 2 };
+
 // Quantizer launchers (quantize.cu).
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, int elem,
                               int layout, uint8_t* codes, uint8_t* scales, int64_t rows_per_mat,
-                              cudaStream_t st);
+                              cudaStream_t st, float* norms = nullptr, int norm_mode = NORM_NONE);
 cudaError_t launch_quant_cols(const uint16_t* x, int64_t batch, int64_t rows, int64_t cols,
                               int elem, int layout, uint8_t* codes, int64_t code_pitch,
                               uint8_t* scales, cudaStream_t st);

@@ -11,6 +11,7 @@
 // Both kernels stream their input once and write codes + scales once: they
 // are HBM-bound, so the design goal is full-sector, coalesced traffic.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fsa_internal.h"
 #include "sm100_ptx.cuh"
@@ -109,6 +110,40 @@ __device__ __forceinline__ int quantize_block32(const uint32_t (&h)[32], int ele
     return X;
 }
 
+// 2^X as an FP32 for X in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int X) {
+    return X >= -126 ? __int_as_float((127 + X) << 23) : __int_as_float(0x00400000);
+}
+
+// Sum of squares of the 32 values of one quantized block: the E4M3 patterns
+// in w (ATTN layout) decoded exactly (E4M3 -> f16 is exact), times 4^X.
+// Overflows to +inf for huge blocks; a block below 2^-60 may round to zero,
+// which the absolute slack of the row bound covers.
+__device__ __forceinline__ float block_sumsq(const uint32_t (&w)[8], int X) {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t f16x2;
+            asm("{\n.reg .b16 t;\ncvt.u16.u32 t, %1;\ncvt.rn.f16x2.e4m3x2 %0, t;\n}"
+                : "=r"(f16x2) : "r"(w[i] >> (16 * h)));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16x2));
+            s = __fmaf_rn(f.x, f.x, s);
+            s = __fmaf_rn(f.y, f.y, s);
+        }
+    }
+    const float p = pow2f(X);
+    return s * p * p;
+}
+
+// Upper bound of a row's Euclidean norm from the FP32 sum of its squares:
+// the relative slack covers the rounding of the 128 squares' sum and of the
+// square root, the absolute one blocks that underflowed.
+__device__ __forceinline__ float norm_bound(float sumsq) {
+    return __fmaf_rn(sqrtf(sumsq), 1.0f + 1.0f / 1024.0f, 1e-18f);
+}
+
 __device__ __forceinline__ int atom_offset(int64_t r_in_tile, int kb) {
     return static_cast<int>((r_in_tile & 31) * 16 + (r_in_tile >> 5) * 4 + kb);
 }
@@ -116,7 +151,8 @@ __device__ __forceinline__ int atom_offset(int64_t r_in_tile, int kb) {
 // Blocks of 32 along the last axis.  One thread per block.
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ x, int64_t lines, int64_t cols,
                                   int elem, int layout, uint8_t* __restrict__ codes,
-                                  uint8_t* __restrict__ scales, int64_t rows_per_mat, int vec) {
+                                  uint8_t* __restrict__ scales, int64_t rows_per_mat, int vec,
+                                  float* __restrict__ norms, int norm_mode) {
     const int64_t nblk = (cols + 31) / 32;
     const int64_t total = lines * nblk;
     const int64_t n_tiles = (rows_per_mat + kTile - 1) / kTile;
@@ -158,6 +194,25 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ x, int64_t lines,
         } else {
             const int64_t mat = line / rows_per_mat, r = line - mat * rows_per_mat;
             scales[(mat * n_tiles + r / kTile) * kAtomBytes + atom_offset(r % kTile, kb)] = sb;
+            if (norm_mode != NORM_NONE) {
+                // the nblk blocks of a row sit in nblk consecutive lanes: the
+                // warp's indices are consecutive, nblk divides 32 and total is
+                // a multiple of nblk, so a row's lanes are active together;
+                // the lanes of this pass are those below total
+                const int64_t base = idx - (threadIdx.x & 31);
+                const int64_t left = total - base;
+                const unsigned act = left >= 32 ? 0xFFFFFFFFu : (1u << left) - 1u;
+                float ss = block_sumsq(w, X);
+                for (int o = 1; o < nblk; o <<= 1) ss += __shfl_xor_sync(act, ss, o);
+                if (kb == 0) {
+                    const float bnd = norm_bound(ss);
+                    if (norm_mode == NORM_ROW)
+                        norms[line] = bnd;
+                    else  // non-negative floats order like their bit patterns
+                        atomicMax(reinterpret_cast<unsigned int*>(norms + mat * n_tiles + r / kTile),
+                                  __float_as_uint(bnd));
+                }
+            }
         }
     }
 }
@@ -214,9 +269,12 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t* __restr
 
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, int elem, int layout,
                               uint8_t* codes, uint8_t* scales, int64_t rows_per_mat,
-                              cudaStream_t st) {
+                              cudaStream_t st, float* norms, int norm_mode) {
     const int64_t total = lines * ((cols + 31) / 32);
     if (total == 0) return cudaSuccess;
+    // row norms need the ATTN layout and whole rows of 2 or 4 blocks in a warp
+    if (norm_mode != NORM_NONE && (layout != QL_ATTN || !norms || (cols != 64 && cols != 128)))
+        return cudaErrorInvalidValue;
     const int vec = (cols % 8 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
                     ((reinterpret_cast<uintptr_t>(codes) & 15) == 0);
     int dev = 0, nsm = 148;
@@ -226,7 +284,8 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, in
     int64_t blocks = (total + threads - 1) / threads;
     blocks = blocks < static_cast<int64_t>(nsm) * 16 ? blocks : static_cast<int64_t>(nsm) * 16;
     quant_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-        x, lines, cols, elem, layout, codes, scales, rows_per_mat > 0 ? rows_per_mat : lines, vec);
+        x, lines, cols, elem, layout, codes, scales, rows_per_mat > 0 ? rows_per_mat : lines, vec,
+        norms, norm_mode);
     return cudaGetLastError();
 }
 
