@@ -218,7 +218,8 @@ FSA_API fsa_status fsa_attention_run(const void *workspace, uint64_t workspace_b
                                      const fsa_options *opt, void *stream);
 
 /* Bytes of device workspace fsa_attention_fwd needs for this shape (MX
- * copies of Q, K, V and their scales).  0 for invalid arguments. */
+ * copies of Q, K, V and their scales, and for MXFP6 / MXFP4 the row-norm
+ * bounds of the quantized Q and K).  0 for invalid arguments. */
 FSA_API uint64_t fsa_attention_workspace_size(int B, int H, int S, int D, int fmt);
 
 /*
