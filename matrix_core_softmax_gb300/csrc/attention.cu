@@ -57,6 +57,15 @@ constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpLoadV = 10, kWarpPv = 11;
 constexpr int kLaunchRegs = 168, kSoftmaxRegs = 232, kHelperRegs = 32;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
+// Work items of at most this many KV tiles go to the persistent kernel
+// (measured on GB300 with 75600 query rows x 40 heads: faster up to 2048
+// keys, even at 4096, slower at 8192).
+constexpr int kPersistentMaxTiles = 16;
+// The persistent kernel's helper warps keep the rings' state across work
+// items and give back only to 40: 2 * 128 * 232 + 128 * 40 = 64512.
+constexpr int kHelperRegsPersistent = 40;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegsPersistent <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kTileBytes = 128 * 128;  // one 128 x 128 byte operand tile
 constexpr int kVBytes = kTileBytes + 16 * 128;  // V^T tile + 16 all-ones rows (row sums)
 constexpr uint32_t kTmemCols = 512;
@@ -65,21 +74,23 @@ constexpr uint32_t kTmemCols = 512;
 // bytes per row), and the scale-factor atoms (4 columns per atom)
 constexpr uint32_t kColS0 = 0, kColO = 256;  // S1 = kColS0 + 128, l = kColO + D
 constexpr uint32_t kColP = 400;              // + 32 * (t & 1)
-constexpr uint32_t kColSfQ = 464, kColSfK = 468 /* +4*(t&1) */, kColSfP = 476 /* +4*(t&1) */,
-                   kColSfV = 484 /* +8*(u&1): V rows 0-127, then unit scales for rows 128-255 */;
-static_assert(kColSfV + 16 <= 512, "TMEM column map beyond the allocation");
+constexpr uint32_t kColSfQ = 464, kColSfK = 468 /* +4*(g&1) */, kColSfP = 476 /* +4*(g&1) */,
+                   kColSfV = 484 /* +8*(g&1): V rows 0-127, then unit scales for rows 128-255 */,
+                   kColSfQ1 = 500 /* persistent kernel: scales of Q buffer 1 */;
+static_assert(kColSfV + 16 <= kColSfQ1 && kColSfQ1 + 4 <= 512, "TMEM column map beyond the allocation");
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic holds rne(x) in its low bits
 
 struct __align__(1024) Smem {
-    uint8_t q[kTileBytes];
+    uint8_t q[2][kTileBytes];  // Q tile (persistent kernel: of its item j in buffer j % 2)
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kVBytes];  // rows [0, D): V^T tile; rows [D, D+16): all ones
-    uint8_t q_sf[kAtomBytes];
+    uint8_t q_sf[2][kAtomBytes];
     uint8_t k_sf[kStages][kAtomBytes];
     uint8_t v_sf[kStages][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
     float tmax_x[8][128];  // row maxima of tile t in slot t % 8, read by the other warpgroup
-    uint64_t bar_q;
+    uint64_t bar_q[2];    // Q tile of buffer i landed
+    uint64_t q_empty[2];  // persistent kernel: score products of the item in Q buffer i retired
     uint64_t k_full[kStages];   // K tile landed
     uint64_t k_empty[kStages];  // score product that read the K tile retired
     uint64_t v_full[kStages];
@@ -89,7 +100,8 @@ struct __align__(1024) Smem {
     uint64_t p_full[kPBuf];
     uint64_t p_free[kPBuf];  // PV of the tile that used P buffer i (and its scales) retired
     uint64_t m_ready[8]; // slot i of tmax_x written (tiles i, i + 8, ...)
-    uint64_t o_full;
+    uint64_t o_full;  // the (item's) last PV product retired
+    uint64_t o_free;  // persistent kernel: the item's O and l read by the epilogue (8 softmax warps)
     uint64_t drain_qk, drain_pv;
     uint32_t tmem_base;
     int abort;
@@ -108,6 +120,7 @@ struct Params {
     unsigned long long* rollback_count;
     unsigned int* err_word;
     int Sq, Sk, D, n_t;  // query rows, keys, head dim, KV tiles ceil(Sk / 128)
+    int n_qt, n_items;   // query tiles ceil(Sq / 128); work items n_qt * B * H
     float sm_scale;  // s = sm_scale * accumulator
     float alpha;     // 128 * log2(e) * sm_scale
     float theta;     // gate threshold, natural-log score units
@@ -499,26 +512,29 @@ __device__ __forceinline__ void rescale_o(uint32_t lane_addr, int D, float resca
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
 template <int kP>
-__device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int it, int wg,
+__device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int g, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
                                              bool row_valid, int64_t grow, bool tail, bool bounded,
                                              RowState& rs) {
     const int D = p.D;
-    const int pb = t & (kPBuf - 1);
+    const int pb = g & (kPBuf - 1);
     bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
     tc_fence_after();
     uint32_t s0[32], s1[32], s2[32], s3[32];
     tmem_ld32(s_col, s0);
     tmem_ld32(s_col + 32, s1);
     // while the scores travel: non-blocking looks at the other warpgroup's
-    // maximum of tile t - 1 and at this tile's P buffer (PV of tile t - 2
-    // retired); both are normally complete by now
-    const int ms = (t - 1) & 7;
-    const uint32_t m_par = ((t - 1) >> 3) & 1;
-    const uint32_t pf_par = ((t >> 1) - 1) & 1;
+    // maximum of tile t - 1 and at this tile's P buffer (PV of the CTA's
+    // tile g - 2 retired); both are normally complete by now.  Buffers,
+    // slots and barrier phases follow the CTA's running tile count g (g = t
+    // when a CTA processes one work item); the method's tile logic follows
+    // t, the tile's index within its work item.
+    const int ms = (g - 1) & 7;
+    const uint32_t m_par = ((g - 1) >> 3) & 1;
+    const uint32_t pf_par = ((g >> 1) - 1) & 1;
     const bool have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
     float prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
-    const bool have_p = t < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
+    const bool have_p = g < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
     tmem_ld_wait();
     tmem_reg_dep(s0);
     tmem_reg_dep(s1);
@@ -561,8 +577,8 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         const float bm0 = tail ? max32(s0) : h_max0, bm1 = tail ? max32(s1) : h_max1;
         const float bm2 = max32(s2), bm3 = max32(s3);
         const float tmax = fmaxf(fmaxf(bm0, bm1), fmaxf(bm2, bm3));
-        sm.tmax_x[t & 7][r] = tmax;
-        warp_arrive(&sm.m_ready[t & 7]);
+        sm.tmax_x[g & 7][r] = tmax;
+        warp_arrive(&sm.m_ready[g & 7]);
         if (t > 0) {
             if (!have_prev) {
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
@@ -575,7 +591,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         rs.m_acc = (t == 0) ? tmax : fmaxf(rs.m_acc, tmax);
         if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
         if (__any_sync(0xFFFFFFFFu, grew)) {
-            ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
+            ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o(lane_addr, D, rescale);
         }
         const uint32_t sb0 = efq_block(s0, bm0, rs.m_acc, p, w0);
@@ -611,12 +627,13 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             }
         }
         const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
-        // publish this tile's row maximum for the other warpgroup in slot t % 8;
-        // the reader consumes it during its tile t + 1, long before this
-        // warpgroup rewrites the slot at tile t + 8 (which needs the reader's
-        // tile t + 7 maximum)
-        sm.tmax_x[t & 7][r] = tmax;
-        warp_arrive(&sm.m_ready[t & 7]);
+        // publish this tile's row maximum for the other warpgroup in slot g % 8;
+        // the reader consumes it during its tile g + 1, long before this
+        // warpgroup rewrites the slot at tile g + 8: the score product of a
+        // tile needs the S buffer the other warpgroup frees two tiles
+        // earlier, so neither warpgroup runs more than a few tiles ahead
+        sm.tmax_x[g & 7][r] = tmax;
+        warp_arrive(&sm.m_ready[g & 7]);
         // frozen reference: replay the gate over the previous tile's maximum,
         // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
         if (t > 0) {
@@ -635,10 +652,10 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             rescale = expf((rs.m_acc - tmax) * p.sm_scale);
             rs.m_acc = tmax;
         }
-        // P buffer pb is free once PV of tile t - 2 retired.  Waited first: PV
-        // products retire in order, so afterwards the barrier of tile t - 1's
-        // buffer is past PV_{t-3} and can only be in the phase of PV_{t-1}
-        // itself (PV_{t+1} needs this tile's P).
+        // P buffer pb is free once PV of tile g - 2 retired.  Waited first: PV
+        // products retire in order, so afterwards the barrier of tile g - 1's
+        // buffer is past PV_{g-3} and can only be in the phase of PV_{g-1}
+        // itself (PV_{g+1} needs this tile's P).
         if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
         if (__any_sync(0xFFFFFFFFu, fire)) {
             // the bitmap was zeroed before the launch: only firings are written
@@ -648,7 +665,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             }
             // recovery: once PV of the previous tile retired, O and l of the
             // firing rows are scaled by exp(m_old - m_new) in TMEM
-            ok &= mbar_wait(&sm.p_free[(t - 1) & 1], ((t - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
+            ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o(lane_addr, D, rescale);
         }
         sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc,
@@ -694,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) {
         sm.abort = 0;
-        mbar_init(&sm.bar_q, 1);
+        mbar_init(&sm.bar_q[0], 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.k_empty[i], 1);
@@ -742,10 +759,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (is_k) {
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
-                mbar_arrive_expect_tx(&sm.bar_q, tile_bytes + kAtomBytes);
-                tma_load_3d(sm.q, &tm_q, &sm.bar_q, 0, q0, bh);
-                bulk_load(sm.q_sf, p.q_sf + (static_cast<int64_t>(bh) * n_qt + qt) * kAtomBytes,
-                          kAtomBytes, &sm.bar_q);
+                mbar_arrive_expect_tx(&sm.bar_q[0], tile_bytes + kAtomBytes);
+                tma_load_3d(sm.q[0], &tm_q, &sm.bar_q[0], 0, q0, bh);
+                bulk_load(sm.q_sf[0], p.q_sf + (static_cast<int64_t>(bh) * n_qt + qt) * kAtomBytes,
+                          kAtomBytes, &sm.bar_q[0]);
             } else {
                 tma_prefetch_desc(&tm_v);
             }
@@ -782,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sm.abort) {
                 // let the copies still in flight land before the CTA exits
                 int dummy = 0;
-                if (is_k) mbar_wait(&sm.bar_q, 0, p.timeout_ns, &dummy);
+                if (is_k) mbar_wait(&sm.bar_q[0], 0, p.timeout_ns, &dummy);
                 for (int t = max(0, issued - kStages); t < issued; ++t) {
                     if (is_k && (p.debug_flags & 1) && t == 1) continue;
                     mbar_wait(&full[t % kStages], (t / kStages) & 1, p.timeout_ns, &dummy);
@@ -805,14 +822,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == kWarpMma) {
                 const uint32_t qk_swz = D == 128 ? SWZ_128B : SWZ_64B;
                 const uint32_t qk_sbo = D == 128 ? 1024u : 512u;
-                const uint64_t dq = smem_desc(smem_u32(sm.q), 16, qk_sbo, qk_swz);
+                const uint64_t dq = smem_desc(smem_u32(sm.q[0]), 16, qk_sbo, qk_swz);
                 const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, qk_sbo, qk_swz);
                 const uint64_t sfk0 = smem_desc(smem_u32(sm.k_sf[0]), 0, 128, SWZ_NONE);
                 constexpr uint32_t id_qk = idesc_mxf8f6f4(128, 128, 0, 0, 0, 0);
-                ok = mbar_wait(&sm.bar_q, 0, p.timeout_ns, &sm.abort);
+                ok = mbar_wait(&sm.bar_q[0], 0, p.timeout_ns, &sm.abort);
                 if (ok) {
                     tc_fence_after();
-                    tc_cp_32x128b_x4(tmem + kColSfQ, smem_desc(smem_u32(sm.q_sf), 0, 128, SWZ_NONE));
+                    tc_cp_32x128b_x4(tmem + kColSfQ, smem_desc(smem_u32(sm.q_sf[0]), 0, 128, SWZ_NONE));
                 }
                 int st = 0;  // K ring stage of tile t
                 for (int t = 0; ok && t < p.n_t; ++t) {
@@ -903,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool bounded = false;
         if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
-            ok = softmax_tile<kP>(sm, p, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail,
+            ok = softmax_tile<kP>(sm, p, t, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail,
                                   bounded, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
@@ -954,6 +971,349 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// Persistent variant for short key sequences (few KV tiles per work item):
+// one CTA per SM walks the work items, so the launch, TMEM allocation and
+// barrier set-up happen once per SM, the next item's Q tile loads into the
+// second Q buffer during the current item, and its first score products run
+// while the current item's output is written.
+template <int kP>
+__global__ void __launch_bounds__(kThreads, 1)
+    fsa_attn_fwd_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the 128-byte-swizzled TMA/MMA tiles need a 1024-byte aligned base
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.err_word, kErrMisaligned);
+        return;
+    }
+    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int D = p.D;
+    const int nkk = D / 32;  // MMA k-steps of the score product
+    // Persistent CTAs: CTA c takes the work items c, c + gridDim.x, ...; item
+    // i is the query tile i % n_qt of head i / n_qt, so at any time the CTAs
+    // work on neighbouring query tiles of the same head (its K and V stay in
+    // L2).  Every role walks the same item sequence; the per-tile buffers
+    // and barrier phases follow the CTA's running tile count.
+
+    // ------------------------------------------------------------- setup
+    if (warp == kWarpMma) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        sm.abort = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.bar_q[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_free[i], 4);  // one arrival per softmax warp
+        }
+        for (int i = 0; i < 8; ++i) mbar_init(&sm.m_ready[i], 4);
+        for (int i = 0; i < kPBuf; ++i) {
+            mbar_init(&sm.p_full[i], 4);
+            mbar_init(&sm.p_free[i], 1);
+        }
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.o_free, 8);  // one arrival per softmax warp after its epilogue read O
+        mbar_init(&sm.drain_qk, 1);
+        mbar_init(&sm.drain_pv, 1);
+        fence_mbar_init();
+    }
+    if (tid < 128) {
+        // 16 all-ones rows (E4M3 1.0 = 0x38) after the D rows of every V^T
+        // stage, so that one PV product of N = D + 16 also yields l = P 1,
+        // and a unit-scale atom (2^0 = 127) for those rows
+        for (int st = 0; st < kStages; ++st)
+            reinterpret_cast<uint4*>(sm.v[st] + p.D * 128)[tid] =
+                make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        reinterpret_cast<uint32_t*>(sm.ones_sf)[tid] = 0x7F7F7F7Fu;
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == kWarpLoad || warp == kWarpLoadV) {
+        warpgroup_reg_dec<kHelperRegsPersistent>();
+        // ------------------------------------------------------ producers
+        // warp 8 loads each item's Q tile (two buffers) and the K ring, warp
+        // 10 the V^T ring; separate rings let K of tile g+3 load as soon as
+        // QK_g retired, long before PV_g releases V.
+        if (lane == 0) {
+            const bool is_k = warp == kWarpLoad;
+            const uint32_t tile_bytes = static_cast<uint32_t>(kTile * D);
+            if (is_k) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+            } else {
+                tma_prefetch_desc(&tm_v);
+            }
+            uint64_t* full = is_k ? sm.k_full : sm.v_full;
+            uint64_t* empty = is_k ? sm.k_empty : sm.v_empty;
+            int issued = 0;    // ring tiles issued (the CTA's running tile count)
+            int q_issued = 0;  // Q tiles issued
+            bool ok = true;
+            int st = 0;        // ring stage of tile g
+            uint32_t ph = 0;   // parity of the ring's current pass
+            for (int item = blockIdx.x, j = 0; ok && item < p.n_items; item += gridDim.x, ++j) {
+                const int bh = item / p.n_qt, qt = item - bh * p.n_qt;
+                if (is_k) {
+                    // Q buffer j % 2 is free once the score products of item j - 2 retired
+                    const int qb = j & 1;
+                    if (j >= 2 && !mbar_wait(&sm.q_empty[qb], ((j >> 1) - 1) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.bar_q[qb], tile_bytes + kAtomBytes);
+                    tma_load_3d(sm.q[qb], &tm_q, &sm.bar_q[qb], 0, qt * kTile, bh);
+                    bulk_load(sm.q_sf[qb], p.q_sf + (static_cast<int64_t>(bh) * p.n_qt + qt) * kAtomBytes,
+                              kAtomBytes, &sm.bar_q[qb]);
+                    q_issued = j + 1;
+                }
+                for (int t = 0; t < p.n_t; ++t) {
+                    if (issued >= kStages && !mbar_wait(&empty[st], ph ^ 1u, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    // test hook: the CTA's K tile 1 never arrives
+                    if (!(is_k && (p.debug_flags & 1) && issued == 1)) {
+                        mbar_arrive_expect_tx(&full[st], tile_bytes + kAtomBytes);
+                        const int64_t a = (static_cast<int64_t>(bh) * p.n_t + t) * kAtomBytes;
+                        if (is_k) {
+                            tma_load_3d(sm.k[st], &tm_k, &full[st], 0, t * kTile, bh);
+                            bulk_load(sm.k_sf[st], p.k_sf + a, kAtomBytes, &full[st]);
+                        } else {
+                            tma_load_3d(sm.v[st], &tm_v, &full[st], t * kTile, 0, bh);
+                            bulk_load(sm.v_sf[st], p.v_sf + a, kAtomBytes, &full[st]);
+                        }
+                    }
+                    ++issued;
+                    if (++st == kStages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) raise_abort(sm, p);
+            if (sm.abort) {
+                // let the copies still in flight land before the CTA exits
+                int dummy = 0;
+                for (int j = max(0, q_issued - 2); j < q_issued; ++j)
+                    mbar_wait(&sm.bar_q[j & 1], (j >> 1) & 1, p.timeout_ns, &dummy);
+                for (int g = max(0, issued - kStages); g < issued; ++g) {
+                    if (is_k && (p.debug_flags & 1) && g == 1) continue;
+                    mbar_wait(&full[g % kStages], (g / kStages) & 1, p.timeout_ns, &dummy);
+                }
+            }
+        }
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        warpgroup_reg_dec<kHelperRegsPersistent>();
+        // ---------------------------------------------------------- MMA
+        // Two issuing threads: warp 9 the score products (into the S
+        // buffers), warp 11 the PV products (into O); a late P therefore never
+        // holds back the next score product.  Descriptors are built once: the
+        // start-address field counts 16-byte units, so + 2 advances an
+        // operand by one 32-byte K step and + 1024 by one 16 KB buffer.
+        if (lane == 0) {
+            constexpr uint32_t kStageUnits = kTileBytes >> 4, kVUnits = kVBytes >> 4,
+                               kAtomUnits = kAtomBytes >> 4;
+#define FSA_SF(kk) ((static_cast<uint32_t>(kk) << 4) | (static_cast<uint32_t>(kk) << 29))
+            bool ok = true;
+            if (warp == kWarpMma) {
+                const uint32_t qk_swz = D == 128 ? SWZ_128B : SWZ_64B;
+                const uint32_t qk_sbo = D == 128 ? 1024u : 512u;
+                const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 16, qk_sbo, qk_swz);
+                const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, qk_sbo, qk_swz);
+                const uint64_t sfq0 = smem_desc(smem_u32(sm.q_sf[0]), 0, 128, SWZ_NONE);
+                const uint64_t sfk0 = smem_desc(smem_u32(sm.k_sf[0]), 0, 128, SWZ_NONE);
+                constexpr uint32_t id_qk = idesc_mxf8f6f4(128, 128, 0, 0, 0, 0);
+                int g = 0;   // the CTA's running tile count
+                int st = 0;  // K ring stage of tile g
+                for (int item = blockIdx.x, j = 0; ok && item < p.n_items; item += gridDim.x, ++j) {
+                    const int qb = j & 1;
+                    if (!mbar_wait(&sm.bar_q[qb], (j >> 1) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfq = tmem + (qb ? kColSfQ1 : kColSfQ);
+                    tc_cp_32x128b_x4(sfq, sfq0 + kAtomUnits * qb);
+                    const uint64_t dq = dq0 + kStageUnits * qb;
+                    for (int t = 0; t < p.n_t; ++t, ++g) {
+                        const int sb = g & 1;
+                        // S buffer sb is free once the softmax of tile g - 2 read it
+                        if (g >= 2 && !mbar_wait(&sm.s_free[sb], ((g - 2) >> 1) & 1, p.timeout_ns, &sm.abort)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(&sm.k_full[st], (g / kStages) & 1, p.timeout_ns, &sm.abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfb = tmem + kColSfK + 4 * sb;
+                        tc_cp_32x128b_x4(sfb, sfk0 + kAtomUnits * st);
+                        const uint64_t bk = dk0 + kStageUnits * st;
+                        const uint32_t dst = tmem + kColS0 + 128 * sb;
+                        mma_mxf8f6f4(dst, dq, bk, id_qk | FSA_SF(0), sfq, sfb, 0u);
+                        mma_mxf8f6f4(dst, dq + 2, bk + 2, id_qk | FSA_SF(1), sfq, sfb, 1u);
+                        if (nkk == 4) {
+                            mma_mxf8f6f4(dst, dq + 4, bk + 4, id_qk | FSA_SF(2), sfq, sfb, 1u);
+                            mma_mxf8f6f4(dst, dq + 6, bk + 6, id_qk | FSA_SF(3), sfq, sfb, 1u);
+                        }
+                        tc_commit(&sm.s_full[sb]);
+                        tc_commit(&sm.k_empty[st]);
+                        st = st + 1 == kStages ? 0 : st + 1;
+                    }
+                    // the item's Q buffer (and its scale copy) is read by now
+                    if (ok) tc_commit(&sm.q_empty[qb]);
+                }
+            } else {
+                const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, SWZ_128B);
+                const uint64_t sfv0 = smem_desc(smem_u32(sm.v_sf[0]), 0, 128, SWZ_NONE);
+                const uint32_t id_pv = idesc_mxf8f6f4(128, D + 16, 0, 0, 0, 0);
+                // unit scales for PV B rows 128-255 (the all-ones rows when D = 128)
+                const uint64_t sf1 = smem_desc(smem_u32(sm.ones_sf), 0, 128, SWZ_NONE);
+                tc_cp_32x128b_x4(tmem + kColSfV + 4, sf1);
+                tc_cp_32x128b_x4(tmem + kColSfV + 12, sf1);
+                int g = 0;   // the CTA's running tile count
+                int st = 0;  // V ring stage of tile g
+                for (int item = blockIdx.x, j = 0; ok && item < p.n_items; item += gridDim.x, ++j) {
+                    // O of the previous item must have been read by the epilogue
+                    if (j > 0 && !mbar_wait(&sm.o_free, (j - 1) & 1, p.timeout_ns, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int u = 0; u < p.n_t; ++u, ++g) {
+                        const int pb = g & (kPBuf - 1);
+                        if (!mbar_wait(&sm.p_full[pb], (g >> 1) & 1, p.timeout_ns, &sm.abort) ||
+                            !mbar_wait(&sm.v_full[st], (g / kStages) & 1, p.timeout_ns, &sm.abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfa = tmem + kColSfP + 4 * pb, sfb = tmem + kColSfV + 8 * (g & 1);
+                        tc_cp_32x128b_x4(sfb, sfv0 + kAtomUnits * st);
+                        // A = P from TMEM: 8 columns per 32-key step
+                        const uint32_t ap = tmem + kColP + 32 * pb;
+                        const uint64_t bv = dv0 + kVUnits * st;
+                        const uint32_t acc = u > 0 ? 1u : 0u;
+                        mma_mxf8f6f4_tmem_a(tmem + kColO, ap, bv, id_pv | FSA_SF(0), sfa, sfb, acc);
+                        mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 8, bv + 2, id_pv | FSA_SF(1), sfa, sfb, 1u);
+                        mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 16, bv + 4, id_pv | FSA_SF(2), sfa, sfb, 1u);
+                        mma_mxf8f6f4_tmem_a(tmem + kColO, ap + 24, bv + 6, id_pv | FSA_SF(3), sfa, sfb, 1u);
+                        tc_commit(&sm.v_empty[st]);
+                        tc_commit(&sm.p_free[pb]);
+                        st = st + 1 == kStages ? 0 : st + 1;
+                    }
+                    if (ok) tc_commit(&sm.o_full);
+                }
+            }
+#undef FSA_SF
+            if (!ok) {
+                raise_abort(sm, p);
+                int dummy = 0;
+                uint64_t* drain = warp == kWarpMma ? &sm.drain_qk : &sm.drain_pv;
+                tc_commit(drain);  // wait until every MMA/copy this thread issued retired
+                mbar_wait(drain, 0, p.timeout_ns, &dummy);
+            }
+        }
+    } else {
+        warpgroup_reg_inc<kSoftmaxRegs>();
+        // ------------------------------------------------------ softmax
+        // Warpgroup wg processes the tiles g with g % 2 == wg (the CTA's
+        // running tile count) in TMEM S buffer wg and P buffer wg; thread r
+        // owns query row r (TMEM lane r).  Tile maxima travel between the
+        // warpgroups through tmax_x / m_ready; each warpgroup replays the
+        // gate over them.  After an item's last PV both warpgroups write
+        // half of its output and release O for the next item.
+        const int wg = warp >> 2;
+        const int r = tid & 127;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = lane_addr + kColS0 + 128 * wg;
+        const int t_tail = (p.Sk % kTile) ? p.n_t - 1 : p.n_t;  // index of a partial last tile
+        bool ok = true;
+        int it = 0;  // tiles this warpgroup processed (phase of its S buffer)
+        RowState rs{0.0f, 0u};  // the firing count runs over all items
+        for (int j = 0; ok; ++j) {
+            const int item = blockIdx.x + j * gridDim.x;
+            if (item >= p.n_items) break;
+            const int g0 = j * p.n_t;  // running count of the item's tile 0
+            const int bh = item / p.n_qt;
+            const int q0 = (item - bh * p.n_qt) * kTile;
+            const bool row_valid = (q0 + r) < p.Sq;
+            const int64_t grow = static_cast<int64_t>(bh) * p.Sq + q0 + r;
+            // six-bit P: a warp whose rows satisfy the norm bound skips the block minima
+            bool bounded = false;
+            if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
+            rs.m_acc = 0.0f;
+            for (int t = (wg - g0) & 1; ok && t < p.n_t; t += 2, ++it)
+                ok = softmax_tile<kP>(sm, p, t, g0 + t, it, wg, r, lane_addr, s_col, row_valid, grow,
+                                      t == t_tail, bounded, rs);
+            if (ok) ok = wait_warp(&sm.o_full, j & 1, p, sm);
+            if (!ok) break;
+            // epilogue: warpgroup wg writes columns [wg * D/2, (wg+1) * D/2)
+            tc_fence_after();
+            uint32_t lv;
+            tmem_ld1(lane_addr + kColO + D, lv);
+            tmem_ld_wait();
+            const float l = __uint_as_float(lv);
+            for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+                uint32_t rr[32];
+                tmem_ld32(lane_addr + kColO + 32 * c, rr);
+                tmem_ld_wait();
+                tmem_reg_dep(rr);
+                if (row_valid) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * jj]), l),
+                                                                  __fdiv_rn(__uint_as_float(rr[2 * jj + 1]), l));
+                        packed[jj] = *reinterpret_cast<uint32_t*>(&h2);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + 32 * c);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        dst[jj] = make_uint4(packed[4 * jj], packed[4 * jj + 1], packed[4 * jj + 2],
+                                             packed[4 * jj + 3]);
+                }
+            }
+            // O and l are read: the next item's first PV product may overwrite them
+            tc_fence_before();
+            warp_arrive(&sm.o_free);
+        }
+        if (!ok) raise_abort(sm, p);
+        if (ok && p.rollback_count) {
+            unsigned tot = rs.fired;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+            if (lane == 0 && tot) atomicAdd(p.rollback_count, static_cast<unsigned long long>(tot));
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
@@ -971,6 +1331,10 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.Sk = a.Sk;
     p.D = a.D;
     p.n_t = (a.Sk + kTile - 1) / kTile;
+    p.n_qt = (a.Sq + kTile - 1) / kTile;
+    const int64_t n_items = static_cast<int64_t>(p.n_qt) * a.BH;
+    if (n_items > INT32_MAX) return cudaErrorInvalidValue;
+    p.n_items = static_cast<int>(n_items);
     p.sm_scale = a.sm_scale;
     p.alpha = static_cast<float>(128.0 * 1.4426950408889634 * static_cast<double>(a.sm_scale));
     p.theta = a.threshold;
@@ -988,21 +1352,40 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
         p.efq_tau = a.efq_tau;
     }
     const size_t smem = sizeof(Smem);
+    int dev = 0, n_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // short key sequences: the per-CTA set-up and pipeline fill would
+    // dominate a CTA that runs only a few KV tiles, so one persistent CTA per
+    // SM walks the work items instead
+    const bool persistent = p.n_t <= kPersistentMaxTiles && n_items > n_sm;
     // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4, E2M1 codes of
     // the EFQ producer for MXFP4-EFQ
-    auto kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<kPE4M3>
-                             : (a.fmt == 3 ? fsa_attn_fwd_kernel<kPEfq> : fsa_attn_fwd_kernel<kPE2M3>);
+    using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
+    KernelFn kernel;
+    if (persistent)
+        kernel = a.fmt == 0 ? fsa_attn_fwd_persistent_kernel<kPE4M3>
+                            : (a.fmt == 3 ? fsa_attn_fwd_persistent_kernel<kPEfq>
+                                          : fsa_attn_fwd_persistent_kernel<kPE2M3>);
+    else
+        kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<kPE4M3>
+                            : (a.fmt == 3 ? fsa_attn_fwd_kernel<kPEfq> : fsa_attn_fwd_kernel<kPE2M3>);
     // the in-kernel register split assumes exactly kLaunchRegs per thread at
     // launch; anything else could make the increase wait forever
     cudaFuncAttributes fa{};
-    cudaError_t ea = cudaFuncGetAttributes(&fa, kernel);
-    if (ea != cudaSuccess) return ea;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>((a.Sq + kTile - 1) / kTile), static_cast<unsigned>(a.BH));
-    kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (persistent) {
+        kernel<<<static_cast<unsigned>(n_sm), kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    } else {
+        dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(a.BH));
+        kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+    }
     return cudaGetLastError();
 }
 
