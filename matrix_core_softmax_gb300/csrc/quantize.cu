@@ -265,6 +265,194 @@ __global__ void __launch_bounds__(256) quant_cols_kernel(const uint16_t* __restr
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Attention layout (E4M3 containers, scale atoms), the fused attention's
+// operands.  Specialised per element type; a row of D = 64 or 128 values has
+// nblk = 2 or 4 blocks, one thread per block, so every index is a shift or a
+// 32-bit division once per block.
+
+// Largest magnitude of 32 bf16 values held as 16 packed pairs (sign bits off,
+// then a 16-bit two-way max: magnitudes order like their bit patterns).
+__device__ __forceinline__ uint32_t amax_pairs(const uint32_t (&u)[16]) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = u[i] & 0x7FFF7FFFu;
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(a));
+    }
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+// bf16 pair -> two FP32 values scaled by sc (exact: sc is a power of two and
+// no bf16 block element drops below the FP32 normal range after scaling).
+__device__ __forceinline__ float2 scale_pair(uint32_t u, float2 sc) {
+    return __fmul2_rn(make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)), sc);
+}
+
+// E4M3 bytes of four E2M1 values: E2M1 -> f16 -> E4M3 are exact conversions.
+__device__ __forceinline__ uint32_t e2m1x4_as_e4m3(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    asm("{\n.reg .b8 n0, n1;\n.reg .b32 h0, h1;\n.reg .b16 e0, e1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 n0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 n1, %4, %3;\n"
+        "cvt.rn.f16x2.e2m1x2 h0, n0;\n"
+        "cvt.rn.f16x2.e2m1x2 h1, n1;\n"
+        "cvt.rn.satfinite.e4m3x2.f16x2 e0, h0;\n"
+        "cvt.rn.satfinite.e4m3x2.f16x2 e1, h1;\n"
+        "mov.b32 %0, {e0, e1};\n}"
+        : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
+
+// Sum of squares of four E4M3 bytes (exact decode to f16, FP32 accumulation).
+__device__ __forceinline__ float sumsq_e4m3x4(uint32_t w, float s) {
+    asm("{\n.reg .b16 p0, p1, a, b, c, d;\n.reg .b32 h0, h1;\n"
+        "mov.b32 {p0, p1}, %1;\n"
+        "cvt.rn.f16x2.e4m3x2 h0, p0;\n"
+        "cvt.rn.f16x2.e4m3x2 h1, p1;\n"
+        "mov.b32 {a, b}, h0;\n"
+        "mov.b32 {c, d}, h1;\n"
+        "fma.rn.f32.f16 %0, a, a, %0;\n"
+        "fma.rn.f32.f16 %0, b, b, %0;\n"
+        "fma.rn.f32.f16 %0, c, c, %0;\n"
+        "fma.rn.f32.f16 %0, d, d, %0;\n}"
+        : "+f"(s) : "r"(w));
+    return s;
+}
+
+// Quantizes one block of 32 bf16 values (16 pairs) into 8 words of E4M3
+// containers; returns the stored scale exponent.  E2M3 values v are stored
+// as the E4M3 pattern of v / 64 with exponent X + 6: rounding to E4M3 there
+// is rounding to E2M3 (the same three mantissa bits, E2M3's subnormal step
+// 1/8 is E4M3's 2^-9 shifted by 2^6), and the products are unchanged.
+template <int kElem>
+__device__ __forceinline__ int quantize_block_attn(const uint32_t (&u)[16], uint32_t (&w)[8]) {
+    constexpr FmtConsts f = kElem == ELEM_E4M3 ? FmtConsts{8, 0x60}
+                                               : (kElem == ELEM_E2M3 ? FmtConsts{2, 0x70} : FmtConsts{2, 0x40});
+    int X = mx_scale_exp(amax_pairs(u), f);
+    if (kElem == ELEM_E2M3 && X <= 121) {
+        const float sc = pow2_neg(X + 6);
+        const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 a = scale_pair(u[2 * i], s2), b = scale_pair(u[2 * i + 1], s2);
+            w[i] = cvt_e4m3x4(a.x, a.y, b.x, b.y);
+        }
+        return X + 6;
+    }
+    const float sc = pow2_neg(X);
+    const float2 s2 = make_float2(sc, sc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 a = scale_pair(u[2 * i], s2), b = scale_pair(u[2 * i + 1], s2);
+        if (kElem == ELEM_E4M3) {
+            w[i] = cvt_e4m3x4(a.x, a.y, b.x, b.y);
+        } else if (kElem == ELEM_E2M1) {
+            w[i] = e2m1x4_as_e4m3(a.x, a.y, b.x, b.y);
+        } else {  // E2M3 block with X > 121 (magnitudes near the bf16 maximum)
+            const uint32_t p0 = to_e4m3_container(ELEM_E2M3, cvt_e2m3x2(a.x, a.y));
+            const uint32_t p1 = to_e4m3_container(ELEM_E2M3, cvt_e2m3x2(b.x, b.y));
+            w[i] = (p0 & 0xFFFFu) | (p1 << 16);
+        }
+    }
+    return X;
+}
+
+// Q and K: lines of D = 64 or 128 bf16 values (lines = B*H*rows), blocks
+// along D.  Optional row-norm bounds (NORM_ROW / NORM_TILE_MAX).
+template <int kElem>
+__global__ void __launch_bounds__(256) quant_rows_attn_kernel(
+    const uint4* __restrict__ x, int lines, int log2_nblk, int rows_per_mat, uint4* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ norms, int norm_mode) {
+    const int nblk = 1 << log2_nblk;
+    const int total = lines << log2_nblk;
+    const int n_tiles = (rows_per_mat + kTile - 1) / kTile;
+    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
+        // a block is 64 bytes of input and 32 of output: uint4 units 4 and 2
+        uint32_t u[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldg(x + 4 * static_cast<int64_t>(idx) + i);
+            u[4 * i] = v.x; u[4 * i + 1] = v.y; u[4 * i + 2] = v.z; u[4 * i + 3] = v.w;
+        }
+        uint32_t w[8];
+        const int X = quantize_block_attn<kElem>(u, w);
+        codes[2 * static_cast<int64_t>(idx)] = make_uint4(w[0], w[1], w[2], w[3]);
+        codes[2 * static_cast<int64_t>(idx) + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int line = idx >> log2_nblk, kb = idx & (nblk - 1);
+        const int mat = line / rows_per_mat, r = line - mat * rows_per_mat;
+        const int64_t tile = static_cast<int64_t>(mat) * n_tiles + (r >> 7);
+        scales[tile * kAtomBytes + atom_offset(r & (kTile - 1), kb)] = static_cast<uint8_t>(X + 127);
+        if (norm_mode != NORM_NONE) {
+            // the nblk blocks of a row sit in nblk consecutive lanes (the
+            // warp's indices are consecutive, nblk divides 32, total is a
+            // multiple of nblk); the lanes of this pass are those below total
+            const int left = total - (idx - static_cast<int>(threadIdx.x & 31));
+            const unsigned act = left >= 32 ? 0xFFFFFFFFu : (1u << left) - 1u;
+            float ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = sumsq_e4m3x4(w[i], ss);
+            const float p2 = pow2f(X);
+            ss = ss * p2 * p2;
+            for (int o = 1; o < nblk; o <<= 1) ss += __shfl_xor_sync(act, ss, o);
+            if (kb == 0) {
+                const float bnd = norm_bound(ss);
+                if (norm_mode == NORM_ROW)
+                    norms[line] = bnd;
+                else  // non-negative floats order like their bit patterns
+                    atomicMax(reinterpret_cast<unsigned int*>(norms + tile), __float_as_uint(bnd));
+            }
+        }
+    }
+}
+
+// V: blocks of 32 keys, written transposed.  A CTA stages 64 keys x D
+// columns with 16-byte loads and each of its threads quantizes one column's
+// block of 32 keys, writing 32 contiguous code bytes of the transposed line.
+constexpr int kColRows = 64;
+template <int kElem>
+__global__ void __launch_bounds__(256) quant_cols_attn_kernel(
+    const uint16_t* __restrict__ x, int rows, int cols, uint8_t* __restrict__ codes, int pitch,
+    uint8_t* __restrict__ scales) {
+    __shared__ __align__(16) uint32_t tile[kColRows][64 + 4];  // bf16 pairs; the pad breaks bank conflicts
+    const int64_t b = blockIdx.y;
+    const int r0 = blockIdx.x * kColRows;
+    const uint16_t* xb = x + b * static_cast<int64_t>(rows) * cols;
+    const int vec_per_row = cols / 8;  // cols = 64 or 128
+    for (int i = threadIdx.x; i < kColRows * vec_per_row; i += blockDim.x) {
+        const int rr = i / vec_per_row, cv = i - rr * vec_per_row;
+        const int r = r0 + rr;
+        const uint4 v = r < rows ? __ldg(reinterpret_cast<const uint4*>(xb + static_cast<int64_t>(r) * cols) + cv)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(&tile[rr][4 * cv]) = v;
+    }
+    __syncthreads();
+    const int c = threadIdx.x % cols, rb = threadIdx.x / cols;  // column, 32-row block of the tile
+    if (rb * 32 >= kColRows || r0 + rb * 32 >= rows) return;
+    // the column's 32 values as 16 pairs (keys 2j, 2j + 1)
+    uint32_t u[16];
+    const int sh = (c & 1) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t lo = (tile[rb * 32 + 2 * j][c >> 1] >> sh) & 0xFFFFu;
+        const uint32_t hi = (tile[rb * 32 + 2 * j + 1][c >> 1] >> sh) & 0xFFFFu;
+        u[j] = lo | (hi << 16);
+    }
+    uint32_t w[8];
+    const int X = quantize_block_attn<kElem>(u, w);
+    const int rblk = r0 + rb * 32;
+    uint4* d4 = reinterpret_cast<uint4*>(codes + (b * cols + c) * static_cast<int64_t>(pitch) + rblk);
+    // pitch is a multiple of 16 and rblk of 32: each 16-byte half of the
+    // block is entirely inside or entirely outside the padded line; the
+    // padding keys [rows, pitch) receive zero codes (loaded as zeros)
+    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    if (rblk + 16 < pitch) d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    const int n_tiles = (rows + kTile - 1) / kTile;
+    scales[(b * n_tiles + rblk / kTile) * kAtomBytes + atom_offset(c, (rblk / 32) & 3)] =
+        static_cast<uint8_t>(X + 127);
+}
+
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, int elem, int layout,
@@ -281,6 +469,27 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t lines, int64_t cols, in
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     const int threads = 256;
+    const int64_t rpm = rows_per_mat > 0 ? rows_per_mat : lines;
+    if (layout == QL_ATTN && vec && (cols == 64 || cols == 128) && total < (int64_t{1} << 31) &&
+        rpm < (int64_t{1} << 31)) {
+        // the fused attention's operands: specialised kernel, 32-bit indexing
+        int64_t blocks = (total + threads - 1) / threads;
+        blocks = blocks < static_cast<int64_t>(nsm) * 8 ? blocks : static_cast<int64_t>(nsm) * 8;
+        const int l2 = cols == 128 ? 2 : 1;
+        const uint4* x4 = reinterpret_cast<const uint4*>(x);
+        uint4* c4 = reinterpret_cast<uint4*>(codes);
+        const int ln = static_cast<int>(lines), rp = static_cast<int>(rpm);
+        if (elem == ELEM_E4M3)
+            quant_rows_attn_kernel<ELEM_E4M3><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+                x4, ln, l2, rp, c4, scales, norms, norm_mode);
+        else if (elem == ELEM_E2M3)
+            quant_rows_attn_kernel<ELEM_E2M3><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+                x4, ln, l2, rp, c4, scales, norms, norm_mode);
+        else
+            quant_rows_attn_kernel<ELEM_E2M1><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+                x4, ln, l2, rp, c4, scales, norms, norm_mode);
+        return cudaGetLastError();
+    }
     int64_t blocks = (total + threads - 1) / threads;
     blocks = blocks < static_cast<int64_t>(nsm) * 16 ? blocks : static_cast<int64_t>(nsm) * 16;
     quant_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
@@ -293,6 +502,20 @@ cudaError_t launch_quant_cols(const uint16_t* x, int64_t batch, int64_t rows, in
                               int elem, int layout, uint8_t* codes, int64_t code_pitch,
                               uint8_t* scales, cudaStream_t st) {
     if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+    if (layout == QL_ATTN && (cols == 64 || cols == 128) && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+        (reinterpret_cast<uintptr_t>(codes) & 15) == 0 && code_pitch % 16 == 0 &&
+        rows < (int64_t{1} << 30) && batch <= 65535) {
+        // the fused attention's V operand: 64-key tiles staged with 16-byte loads
+        dim3 g(static_cast<unsigned>((rows + kColRows - 1) / kColRows), static_cast<unsigned>(batch));
+        const int r = static_cast<int>(rows), c = static_cast<int>(cols), pt = static_cast<int>(code_pitch);
+        if (elem == ELEM_E4M3)
+            quant_cols_attn_kernel<ELEM_E4M3><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+        else if (elem == ELEM_E2M3)
+            quant_cols_attn_kernel<ELEM_E2M3><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+        else
+            quant_cols_attn_kernel<ELEM_E2M1><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+        return cudaGetLastError();
+    }
     dim3 grid(static_cast<unsigned>((rows + 31) / 32),
               static_cast<unsigned>((cols + kColTileC - 1) / kColTileC),
               static_cast<unsigned>(batch));
