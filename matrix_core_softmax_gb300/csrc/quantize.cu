@@ -396,61 +396,69 @@ __global__ void __launch_bounds__(256) quant_rows_attn_kernel(
             const float p2 = pow2f(X);
             ss = ss * p2 * p2;
             for (int o = 1; o < nblk; o <<= 1) ss += __shfl_xor_sync(act, ss, o);
-            if (kb == 0) {
-                const float bnd = norm_bound(ss);
-                if (norm_mode == NORM_ROW)
-                    norms[line] = bnd;
-                else  // non-negative floats order like their bit patterns
-                    atomicMax(reinterpret_cast<unsigned int*>(norms + tile), __float_as_uint(bnd));
+            const float bnd = norm_bound(ss);  // every lane of the row holds it
+            if (norm_mode == NORM_ROW) {
+                if (kb == 0) norms[line] = bnd;
+            } else {
+                // one atomic per KV tile and warp: the lanes of a tile take
+                // their maximum first (non-negative floats order like their
+                // bit patterns)
+                const unsigned grp = __match_any_sync(act, tile);
+                const unsigned m = __reduce_max_sync(grp, __float_as_uint(bnd));
+                if ((threadIdx.x & 31) == __ffs(grp) - 1)
+                    atomicMax(reinterpret_cast<unsigned int*>(norms + tile), m);
             }
         }
     }
 }
 
-// V: blocks of 32 keys, written transposed.  A CTA stages 64 keys x D
-// columns with 16-byte loads and each of its threads quantizes one column's
-// block of 32 keys, writing 32 contiguous code bytes of the transposed line.
-constexpr int kColRows = 64;
+// V: blocks of 32 keys, written transposed.  One thread per pair of
+// columns and 32 keys: 32 four-byte loads (a warp reads 128 contiguous bytes
+// of a key row per load), the two columns split by byte permutes, two blocks
+// quantized, 32 contiguous code bytes written to each of the two transposed
+// lines.
 template <int kElem>
 __global__ void __launch_bounds__(256) quant_cols_attn_kernel(
-    const uint16_t* __restrict__ x, int rows, int cols, uint8_t* __restrict__ codes, int pitch,
-    uint8_t* __restrict__ scales) {
-    __shared__ __align__(16) uint32_t tile[kColRows][64 + 4];  // bf16 pairs; the pad breaks bank conflicts
-    const int64_t b = blockIdx.y;
-    const int r0 = blockIdx.x * kColRows;
-    const uint16_t* xb = x + b * static_cast<int64_t>(rows) * cols;
-    const int vec_per_row = cols / 8;  // cols = 64 or 128
-    for (int i = threadIdx.x; i < kColRows * vec_per_row; i += blockDim.x) {
-        const int rr = i / vec_per_row, cv = i - rr * vec_per_row;
-        const int r = r0 + rr;
-        const uint4 v = r < rows ? __ldg(reinterpret_cast<const uint4*>(xb + static_cast<int64_t>(r) * cols) + cv)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(&tile[rr][4 * cv]) = v;
-    }
-    __syncthreads();
-    const int c = threadIdx.x % cols, rb = threadIdx.x / cols;  // column, 32-row block of the tile
-    if (rb * 32 >= kColRows || r0 + rb * 32 >= rows) return;
-    // the column's 32 values as 16 pairs (keys 2j, 2j + 1)
-    uint32_t u[16];
-    const int sh = (c & 1) * 16;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint32_t lo = (tile[rb * 32 + 2 * j][c >> 1] >> sh) & 0xFFFFu;
-        const uint32_t hi = (tile[rb * 32 + 2 * j + 1][c >> 1] >> sh) & 0xFFFFu;
-        u[j] = lo | (hi << 16);
-    }
-    uint32_t w[8];
-    const int X = quantize_block_attn<kElem>(u, w);
-    const int rblk = r0 + rb * 32;
-    uint4* d4 = reinterpret_cast<uint4*>(codes + (b * cols + c) * static_cast<int64_t>(pitch) + rblk);
-    // pitch is a multiple of 16 and rblk of 32: each 16-byte half of the
-    // block is entirely inside or entirely outside the padded line; the
-    // padding keys [rows, pitch) receive zero codes (loaded as zeros)
-    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    if (rblk + 16 < pitch) d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    const uint32_t* __restrict__ x, int batch, int rows, int log2_cpairs, uint8_t* __restrict__ codes,
+    int pitch, uint8_t* __restrict__ scales) {
+    const int cpairs = 1 << log2_cpairs;  // D / 2 = 32 or 64
+    const int cols = 2 * cpairs;
+    const int rblocks = (rows + 31) / 32;
     const int n_tiles = (rows + kTile - 1) / kTile;
-    scales[(b * n_tiles + rblk / kTile) * kAtomBytes + atom_offset(c, (rblk / 32) & 3)] =
-        static_cast<uint8_t>(X + 127);
+    const int total = (batch * rblocks) << log2_cpairs;  // < 2^31, checked by the launcher
+    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += gridDim.x * blockDim.x) {
+        const int cp = g & (cpairs - 1);
+        const int t = g >> log2_cpairs;
+        const int b32 = t / rblocks;
+        const int rb = t - b32 * rblocks;
+        const int64_t b = b32;
+        const int r0 = rb * 32;
+        const uint32_t* src = x + (b * rows + r0) * cpairs + cp;
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = r0 + j < rows ? __ldg(src + static_cast<int64_t>(j) * cpairs) : 0u;
+        uint32_t u0[16], u1[16];  // columns 2 cp and 2 cp + 1 as pairs of keys (2j, 2j + 1)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            u0[j] = __byte_perm(w[2 * j], w[2 * j + 1], 0x5410);
+            u1[j] = __byte_perm(w[2 * j], w[2 * j + 1], 0x7632);
+        }
+        // pitch is a multiple of 16 and r0 of 32: each 16-byte half of a
+        // block is entirely inside or entirely outside the padded line; the
+        // padding keys [rows, pitch) receive zero codes (loaded as zeros)
+        const int kb = rb & 3;
+        const int64_t atom = (b * n_tiles + r0 / kTile) * kAtomBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t q[8];
+            const int X = quantize_block_attn<kElem>(h ? u1 : u0, q);
+            const int c = 2 * cp + h;
+            uint4* d4 = reinterpret_cast<uint4*>(codes + (b * cols + c) * static_cast<int64_t>(pitch) + r0);
+            d4[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            if (r0 + 16 < pitch) d4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            scales[atom + atom_offset(c, kb)] = static_cast<uint8_t>(X + 127);
+        }
+    }
 }
 
 }  // namespace
@@ -504,16 +512,24 @@ cudaError_t launch_quant_cols(const uint16_t* x, int64_t batch, int64_t rows, in
     if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
     if (layout == QL_ATTN && (cols == 64 || cols == 128) && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
         (reinterpret_cast<uintptr_t>(codes) & 15) == 0 && code_pitch % 16 == 0 &&
-        rows < (int64_t{1} << 30) && batch <= 65535) {
-        // the fused attention's V operand: 64-key tiles staged with 16-byte loads
-        dim3 g(static_cast<unsigned>((rows + kColRows - 1) / kColRows), static_cast<unsigned>(batch));
-        const int r = static_cast<int>(rows), c = static_cast<int>(cols), pt = static_cast<int>(code_pitch);
+        code_pitch < (int64_t{1} << 31) && batch * ((rows + 31) / 32) * (cols / 2) < (int64_t{1} << 31)) {
+        // the fused attention's V operand: a thread per column pair and 32 keys
+        int dev = 0, nsm = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t total = batch * ((rows + 31) / 32) * (cols / 2);
+        int64_t blocks = (total + 255) / 256;
+        blocks = blocks < static_cast<int64_t>(nsm) * 8 ? blocks : static_cast<int64_t>(nsm) * 8;
+        const uint32_t* x2 = reinterpret_cast<const uint32_t*>(x);
+        const int bt = static_cast<int>(batch), r = static_cast<int>(rows), pt = static_cast<int>(code_pitch);
+        const int l2 = cols == 128 ? 6 : 5;
+        const unsigned nb = static_cast<unsigned>(blocks);
         if (elem == ELEM_E4M3)
-            quant_cols_attn_kernel<ELEM_E4M3><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E4M3><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
         else if (elem == ELEM_E2M3)
-            quant_cols_attn_kernel<ELEM_E2M3><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E2M3><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
         else
-            quant_cols_attn_kernel<ELEM_E2M1><<<g, 256, 0, st>>>(x, r, c, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E2M1><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
         return cudaGetLastError();
     }
     dim3 grid(static_cast<unsigned>((rows + 31) / 32),
