@@ -258,6 +258,45 @@ FSA_API fsa_status fsa_attention_fwd_noalloc(const void *q, const void *k, const
                                              int B, int H, int S, int D, int fmt,
                                              float threshold, void *stream);
 
+/*
+ * fsa_attention_fwd_host / fsa_cross_attention_fwd_host -- the fused
+ * attention on HOST buffers.  (An addition of this library; the pages have
+ * no counterpart.)
+ *
+ * q, o: host bf16 [B][H][Sq][D]; k, v: host bf16 [B][H][Sk][D] (Sq = Sk = S
+ * for the self-attention form).  Same formats, threshold, options and
+ * results as fsa_cross_attention_fwd; opt->rollback_bits and
+ * opt->rollback_count stay DEVICE pointers, opt->workspace is ignored.
+ *  - The heads are streamed through the device in chunks (about eight, each
+ *    at least two waves of query tiles): while one chunk's quantizer and
+ *    fused kernel run, the next chunk's q, k, v are copied in and the
+ *    previous chunk's output copied out, on two copy streams of the library;
+ *    consecutive chunks compute on `stream` and on a second stream of the
+ *    library, so that their kernels overlap.
+ *  - Page-locked host memory (cudaHostAlloc, cudaHostRegister) lets the
+ *    copies run asynchronously and overlap; pageable memory gives the same
+ *    results with copies that block the calling thread.
+ *  - Asynchronous like the other calls: the work is ordered after what was
+ *    already enqueued on `stream`, and `stream` waits for all of it, so o is
+ *    complete once `stream` has been synchronised.  The caller keeps q, k,
+ *    v unchanged and o unread until then.
+ *  - Device memory: two chunk buffer sets (bf16 inputs and output of a
+ *    chunk plus its MX workspace), cached per device, grown on demand
+ *    (synchronising), freed by fsa_release_workspace.  Host-side use is
+ *    serialised by a per-device lock; calls on different streams are
+ *    ordered on the GPU through the library's events.
+ *  - Errors: as fsa_cross_attention_fwd (no pointer alignment is required
+ *    of the host buffers); FSA_ERR_OUT_OF_MEMORY if the chunk buffers cannot
+ *    be allocated, FSA_ERR_CUDA if a copy, event or launch fails.
+ */
+FSA_API fsa_status fsa_attention_fwd_host(const void *q, const void *k, const void *v, void *o,
+                                          int B, int H, int S, int D, int fmt, float threshold,
+                                          const fsa_options *opt, void *stream);
+FSA_API fsa_status fsa_cross_attention_fwd_host(const void *q, const void *k, const void *v, void *o,
+                                                int B, int H, int Sq, int Sk, int D, int fmt,
+                                                float threshold, const fsa_options *opt,
+                                                void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: FSA_OK, FSA_ERR_TIMEOUT, or FSA_ERR_CUDA if the sync
  * itself failed. */
@@ -266,7 +305,8 @@ FSA_API fsa_status fsa_get_device_error(void *stream);
 /* Static description of a status code. */
 FSA_API const char *fsa_status_string(fsa_status s);
 
-/* Frees the library's cached workspaces on every device (synchronising). */
+/* Frees the library's cached workspaces (including the host-buffer entry
+ * points' chunk buffers) on every device (synchronising). */
 FSA_API void fsa_release_workspace(void);
 
 #ifdef __cplusplus

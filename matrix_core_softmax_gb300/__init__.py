@@ -29,7 +29,8 @@ EXPORTS = ("fsa_quantize_mx", "fsa_attention_fwd", "fsa_attention_fwd_ex",
            "fsa_attention_prepare", "fsa_attention_run", "fsa_attention_workspace_size", "fsa_bf16_attention_fwd", "fsa_get_device_error",
            "fsa_status_string", "fsa_release_workspace", "fsa_attention_fwd_noalloc",
            "fsa_cross_attention_fwd", "fsa_cross_attention_workspace_size",
-           "fsa_cross_attention_prepare", "fsa_cross_attention_run")
+           "fsa_cross_attention_prepare", "fsa_cross_attention_run",
+           "fsa_attention_fwd_host", "fsa_cross_attention_fwd_host")
 
 
 class FsaError(RuntimeError):
@@ -91,6 +92,12 @@ def load(path: str | None = None):
             lib.fsa_cross_attention_run.argtypes = [V, ctypes.c_uint64, V, I, I, I, I, I, I, F,
                                                     ctypes.POINTER(Options), V]
             lib.fsa_cross_attention_run.restype = I
+            lib.fsa_attention_fwd_host.argtypes = [V, V, V, V, I, I, I, I, I, F,
+                                                   ctypes.POINTER(Options), V]
+            lib.fsa_attention_fwd_host.restype = I
+            lib.fsa_cross_attention_fwd_host.argtypes = [V, V, V, V, I, I, I, I, I, I, F,
+                                                         ctypes.POINTER(Options), V]
+            lib.fsa_cross_attention_fwd_host.restype = I
             lib.fsa_attention_fwd_noalloc.argtypes = [V, V, V, V, I, I, I, I, I, F, V]
             lib.fsa_attention_fwd_noalloc.restype = I
             lib.fsa_bf16_attention_fwd.argtypes = [V, V, V, V, I, I, I, I, V]
@@ -200,6 +207,66 @@ def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, 
     _check(load().fsa_cross_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
                                           FORMATS[fmt], float(threshold), ctypes.byref(opt),
                                           _stream(stream)), "fsa_cross_attention_fwd")
+    return o
+
+
+def _host_bhsd(t, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda or t.dim() != 4 \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host (CPU) bf16 tensor [B, H, S, D]")
+
+
+def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
+                             sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
+                             efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+    """fsa_cross_attention_fwd_host: q, k, v contiguous HOST bf16 tensors
+    ([B, H, Sq, D] and [B, H, Sk, D]; pinned memory lets the copies overlap
+    the computation); returns the host output o [B, H, Sq, D] (or fills
+    `out`).  Asynchronous on `stream`: synchronise it before reading o.
+    rollback_bits / rollback_count, when given, are CUDA tensors."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _host_bhsd(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if k.shape != (B, H, Sk, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Sk, D] with q's B, H and D")
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned()) if out is None else out
+    _host_bhsd(o, "out")
+    if o.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    opt = Options()
+    opt.sm_scale = sm_scale
+    opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
+    opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    _check(load().fsa_cross_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
+                                               FORMATS[fmt], float(threshold), ctypes.byref(opt),
+                                               _stream(stream)), "fsa_cross_attention_fwd_host")
+    return o
+
+
+def attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
+                       sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
+                       efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+    """fsa_attention_fwd_host: self-attention on contiguous HOST bf16 tensors
+    [B, H, S, D]; see cross_attention_fwd_host."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _host_bhsd(t, n)
+    B, H, S, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have one shape [B, H, S, D]")
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=q.is_pinned()) if out is None else out
+    _host_bhsd(o, "out")
+    if o.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    opt = Options()
+    opt.sm_scale = sm_scale
+    opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
+    opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
+    opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    _check(load().fsa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
+                                         FORMATS[fmt], float(threshold), ctypes.byref(opt),
+                                         _stream(stream)), "fsa_attention_fwd_host")
     return o
 
 

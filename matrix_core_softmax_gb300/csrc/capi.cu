@@ -13,12 +13,26 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Library-owned resources of the host-buffer entry points: two chunk buffer
+// sets (bf16 Q, K, V and O of a chunk of heads plus the chunk's MX
+// workspace), a copy-in and a copy-out stream, a second compute stream, and
+// the events that order them.
+struct HostPipe {
+    void* buf = nullptr;
+    size_t bytes = 0;
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp1 = nullptr;
+    cudaEvent_t in_ready[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {};
+    cudaEvent_t start = nullptr, copies_done = nullptr, comp1_done = nullptr;
+    bool init = false;
+};
+
 struct DeviceState {
     std::mutex mu;
     void* ws = nullptr;
     size_t ws_bytes = 0;
     unsigned int* err = nullptr;
     int arch_ok = -1;  // -1 unknown, 0 no, 1 yes
+    HostPipe hp;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -228,6 +242,122 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int Sq, int Sk, int D, i
     return launch_fsa_attention(a, st) == cudaSuccess ? FSA_OK : FSA_ERR_CUDA;
 }
 
+// Lazily creates the streams and events of the host-buffer pipeline.
+fsa_status host_pipe_init(HostPipe& hp) {
+    if (hp.init) return FSA_OK;
+    if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.comp1, cudaStreamNonBlocking) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    cudaEvent_t* evs[] = {&hp.in_ready[0], &hp.in_ready[1], &hp.in_free[0], &hp.in_free[1],
+                          &hp.out_ready[0], &hp.out_ready[1], &hp.out_free[0], &hp.out_free[1],
+                          &hp.start, &hp.copies_done, &hp.comp1_done};
+    for (cudaEvent_t* e : evs)
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return FSA_ERR_CUDA;
+    hp.init = true;
+    return FSA_OK;
+}
+
+// Heads per chunk of the host-buffer pipeline: about eight chunks, each at
+// least two waves of 152-SM query-tile CTAs, never more heads than exist.
+int64_t host_chunk_heads(int64_t BH, int Sq) {
+    const int64_t n_qt = (static_cast<int64_t>(Sq) + kTile - 1) / kTile;
+    int64_t g = (BH + 7) / 8;
+    const int64_t min_g = (304 + n_qt - 1) / n_qt;
+    if (g < min_g) g = min_g;
+    return g < BH ? g : BH;
+}
+
+// The attention of host-resident q, k, v into host o, streamed through the
+// device in chunks of heads.  Chunk c uses buffer set c % 2 and runs its
+// quantizer and fused kernel on the caller's stream (even c) or the
+// library's second compute stream (odd c), so consecutive chunks' kernels
+// overlap at their tails; its inputs are copied in on the copy-in stream
+// while the previous chunk computes, and its output copied out on the
+// copy-out stream while the next one computes.  Each buffer's reuse waits
+// on the event of its last reader.  The caller's stream finally waits for
+// the last copy-out and the second compute stream.
+fsa_status host_fwd_impl(DeviceState& ds, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         uint16_t* o, int64_t BH, int Sq, int Sk, int D, int fmt, float threshold,
+                         const fsa_options& op, cudaStream_t st) {
+    HostPipe& hp = ds.hp;
+    fsa_status s = host_pipe_init(hp);
+    if (s != FSA_OK) return s;
+    const int64_t G = host_chunk_heads(BH, Sq);
+    const size_t q_bytes = static_cast<size_t>(G) * Sq * D * 2, kv_bytes = static_cast<size_t>(G) * Sk * D * 2;
+    const size_t ws_bytes = attn_workspace_bytes(G, Sq, Sk, D);
+    const size_t set_bytes = 2 * align256(q_bytes) + 2 * align256(kv_bytes) + align256(ws_bytes);
+    if (hp.bytes < 2 * set_bytes) {
+        if (hp.buf) {
+            cudaDeviceSynchronize();
+            cudaFree(hp.buf);
+            hp.buf = nullptr;
+            hp.bytes = 0;
+        }
+        if (cudaMalloc(&hp.buf, 2 * set_bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return FSA_ERR_OUT_OF_MEMORY;
+        }
+        hp.bytes = 2 * set_bytes;
+    }
+    uint8_t* dq[2], *dk[2], *dv[2], *dout[2], *dws[2];
+    for (int i = 0; i < 2; ++i) {
+        uint8_t* p = static_cast<uint8_t*>(hp.buf) + i * set_bytes;
+        dq[i] = p; p += align256(q_bytes);
+        dout[i] = p; p += align256(q_bytes);
+        dk[i] = p; p += align256(kv_bytes);
+        dv[i] = p; p += align256(kv_bytes);
+        dws[i] = p;
+    }
+    // everything already on the caller's stream comes first
+    if (cudaEventRecord(hp.start, st) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.comp1, hp.start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp.d2h, hp.start, 0) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    const int64_t n_t = (static_cast<int64_t>(Sk) + kTile - 1) / kTile;
+    for (int64_t h0 = 0, c = 0; h0 < BH; h0 += G, ++c) {
+        const int i = static_cast<int>(c & 1);
+        const int64_t g = BH - h0 < G ? BH - h0 : G;
+        const size_t qb = static_cast<size_t>(g) * Sq * D * 2, kb = static_cast<size_t>(g) * Sk * D * 2;
+        const size_t qo = static_cast<size_t>(h0) * Sq * D, ko = static_cast<size_t>(h0) * Sk * D;
+        cudaStream_t cs = i ? hp.comp1 : st;
+        // copy in once the quantizer of the chunk two back has read the buffers
+        if (cudaStreamWaitEvent(hp.h2d, hp.in_free[i], 0) != cudaSuccess ||
+            cudaMemcpyAsync(dq[i], q + qo, qb, cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess ||
+            cudaMemcpyAsync(dk[i], k + ko, kb, cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess ||
+            cudaMemcpyAsync(dv[i], v + ko, kb, cudaMemcpyHostToDevice, hp.h2d) != cudaSuccess ||
+            cudaEventRecord(hp.in_ready[i], hp.h2d) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        // quantize (once the inputs landed and the last fused kernel that read
+        // this workspace -- possibly a previous call's on another stream --
+        // finished), then attend once the copy-out of the chunk two back is done
+        if (cudaStreamWaitEvent(cs, hp.in_ready[i], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, hp.out_ready[i], 0) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        s = prepare_impl(dq[i], dk[i], dv[i], g, Sq, Sk, D, fmt, dws[i], cs);
+        if (s != FSA_OK) return s;
+        if (cudaEventRecord(hp.in_free[i], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, hp.out_free[i], 0) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        fsa_options oc = op;
+        oc.rollback_bits = op.rollback_bits ? op.rollback_bits + static_cast<size_t>(h0) * Sq * n_t : nullptr;
+        s = run_impl(dws[i], dout[i], g, Sq, Sk, D, fmt, threshold, oc, ds.err, cs);
+        if (s != FSA_OK) return s;
+        if (cudaEventRecord(hp.out_ready[i], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.d2h, hp.out_ready[i], 0) != cudaSuccess ||
+            cudaMemcpyAsync(o + qo, dout[i], qb, cudaMemcpyDeviceToHost, hp.d2h) != cudaSuccess ||
+            cudaEventRecord(hp.out_free[i], hp.d2h) != cudaSuccess)
+            return FSA_ERR_CUDA;
+    }
+    if (cudaEventRecord(hp.copies_done, hp.d2h) != cudaSuccess ||
+        cudaEventRecord(hp.comp1_done, hp.comp1) != cudaSuccess ||
+        cudaStreamWaitEvent(st, hp.copies_done, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(st, hp.comp1_done, 0) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    return FSA_OK;
+}
+
 }  // namespace
 }  // namespace fsa
 
@@ -382,6 +512,36 @@ fsa_status fsa_cross_attention_fwd(const void* q, const void* k, const void* v, 
     return run_impl(ds->ws, o, BH, Sq, Sk, D, fmt, threshold, op, ds->err, st);
 }
 
+fsa_status fsa_cross_attention_fwd_host(const void* q, const void* k, const void* v, void* o, int B,
+                                        int H, int Sq, int Sk, int D, int fmt, float threshold,
+                                        const fsa_options* opt, void* stream) {
+    if (!q || !k || !v || !o) return FSA_ERR_INVALID_ARGUMENT;
+    if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FSA_ERR_INVALID_ARGUMENT;
+    if (D != 64 && D != 128) return FSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * H > 65535) return FSA_ERR_INVALID_ARGUMENT;
+    if (Sq > (1 << 30) || Sk > (1 << 30)) return FSA_ERR_INVALID_ARGUMENT;
+    fsa_options defaults{};
+    const fsa_options& op = opt ? *opt : defaults;
+    fsa_status s = check_run_args(fmt, threshold, op);
+    if (s != FSA_OK) return s;
+    int dev;
+    DeviceState* ds;
+    s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    // the lock serialises host-side use of the library's buffers, streams and events
+    std::lock_guard<std::mutex> lk(ds->mu);
+    return host_fwd_impl(*ds, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+                         static_cast<const uint16_t*>(v), static_cast<uint16_t*>(o),
+                         static_cast<int64_t>(B) * H, Sq, Sk, D, fmt, threshold, op,
+                         static_cast<cudaStream_t>(stream));
+}
+
+fsa_status fsa_attention_fwd_host(const void* q, const void* k, const void* v, void* o, int B, int H,
+                                  int S, int D, int fmt, float threshold, const fsa_options* opt,
+                                  void* stream) {
+    return fsa_cross_attention_fwd_host(q, k, v, o, B, H, S, S, D, fmt, threshold, opt, stream);
+}
+
 fsa_status fsa_attention_fwd(const void* q, const void* k, const void* v, void* o, int B, int H,
                              int S, int D, int fmt, float threshold, void* stream) {
     return fsa_attention_fwd_ex(q, k, v, o, B, H, S, D, fmt, threshold, nullptr, stream);
@@ -446,12 +606,15 @@ void fsa_release_workspace(void) {
     cudaGetDevice(&cur);
     for (int d = 0; d < n && d < kMaxDevices; ++d) {
         std::lock_guard<std::mutex> lk(g_dev[d].mu);
-        if (g_dev[d].ws) {
+        if (g_dev[d].ws || g_dev[d].hp.buf) {
             cudaSetDevice(d);
             cudaDeviceSynchronize();
             cudaFree(g_dev[d].ws);
             g_dev[d].ws = nullptr;
             g_dev[d].ws_bytes = 0;
+            cudaFree(g_dev[d].hp.buf);
+            g_dev[d].hp.buf = nullptr;
+            g_dev[d].hp.bytes = 0;
         }
     }
     cudaSetDevice(cur);
