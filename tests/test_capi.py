@@ -101,3 +101,36 @@ def test_quantize_argument_validation(lib):
     assert lib.fsa_quantize_mx(P(17), 1, 4, 4, 1, 0, P(16), P(16), None) == 1
     # empty tensor: nothing to do, no device needed
     assert lib.fsa_quantize_mx(P(16), 0, 4, 4, 1, 0, P(16), P(16), None) == 0
+
+
+def test_host_attention_argument_validation(lib):
+    # host-buffer entry points: shape, format and threshold checks happen on
+    # the host before any device call (host pointers need no alignment)
+    P = ctypes.c_void_p
+
+    def host(q=16, B=1, H=1, Sq=8, Sk=8, D=64, fmt=0, theta=8.0):
+        return lib.fsa_cross_attention_fwd_host(P(q) if q else None, P(16), P(16), P(16), B, H, Sq, Sk,
+                                                D, fmt, theta, None, None)
+    assert host(q=0) == 1
+    assert host(Sq=0) == 1
+    assert host(Sk=-1) == 1
+    assert host(D=96) == 2
+    assert host(fmt=4) == 1
+    assert host(theta=float("inf")) == 1
+    assert host(B=300, H=300) == 1
+    assert lib.fsa_attention_fwd_host(None, P(16), P(16), P(16), 1, 1, 8, 64, 0, 8.0, None, None) == 1
+    assert lib.fsa_attention_fwd_host(P(16), P(16), P(16), P(16), 1, 1, 8, 80, 0, 8.0, None, None) == 2
+
+
+def test_host_attention_binding_rejects_device_or_mismatched_tensors():
+    import torch
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fsa.attention_fwd_host(q, q, q.float())                      # not bf16
+    with pytest.raises(ValueError):
+        fsa.attention_fwd_host(q, q, torch.zeros(1, 2, 9, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        fsa.cross_attention_fwd_host(q, torch.zeros(1, 2, 5, 64, dtype=torch.bfloat16),
+                                     torch.zeros(1, 2, 6, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        fsa.attention_fwd_host(q, q, q, out=torch.zeros(1, 2, 8, 32, dtype=torch.bfloat16))
