@@ -338,10 +338,14 @@ __device__ __forceinline__ float linear_kx(int sb) { return __int_as_float(0x4D3
 __device__ __forceinline__ float linear_kx2(int sb) { return __int_as_float(0x4D3372F8 - 8 * sb); }
 
 // One arrival per warp: the lanes' preceding shared-memory writes and TMEM
-// reads are ordered before lane 0's release-arrive by the warp barrier.
+// reads are ordered before lane 0's release-arrive by the warp barrier.  The
+// arrive is predicated on lane 0 inside the asm, so the warp takes no
+// branch (a divergent lane-0 region would cost a convergence barrier).
 __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    asm volatile("{\n.reg .pred p;\nsetp.eq.u32 p, %0, 0;\n"
+                 "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%1];\n}"
+                 :: "r"(threadIdx.x & 31), "r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Params& p, Smem& sm) {
