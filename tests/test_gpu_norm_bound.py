@@ -1,4 +1,5 @@
-"""GPU parity of the six-bit P conversion at the edges of its norm bound.
+"""GPU parity of the six-bit P conversion at the edges of its norm bound, and
+of operands at the edge of the scale range.
 
 For MXFP6 and MXFP4 the fused kernel skips the block minima for a warp whose
 rows satisfy 2 |alpha| |q^_i| max_j |k^_j| <= 15000 (alpha = 128 log2(e) sm),
@@ -91,3 +92,17 @@ def test_one_large_key_tile_unbounds_the_head(fsa, fmt):
     kf[0, 1, 515, :] *= np.float32(30.0)
     k = fsa_inputs.to_bf16_bits(kf)
     _check(fsa, q, k, v, fmt, theta=80.0)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp6", "mxfp4", "mxfp8"])
+def test_near_bf16_maximum_values_in_v(fsa, fmt):
+    # one key row of V at 2^126 (scale exponent X > 121: the six-bit
+    # quantizer keeps the exact decode there instead of the v / 64 pattern
+    # with exponent X + 6, which E8M0 could not hold); the output stays
+    # finite because that key carries one weight among many
+    B, H, S, D = 1, 2, 700, 128
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=88)
+    vf = fsa_inputs.bf16_bits_to_f32(v)
+    vf[0, 0, 333, :] = np.float32(2.0 ** 126) * np.sign(vf[0, 0, 333, :] + 0.5)
+    v = fsa_inputs.to_bf16_bits(vf)
+    _check(fsa, q, k, v, fmt)
