@@ -198,11 +198,23 @@ def aggregate_tflops(world, flops_per_call, n_calls, elapsed_s):
     return world * flops_per_call * n_calls / elapsed_s / 1e12
 
 
+def cpu_affinity():
+    """Cores this process may run on: their count and the affinity list as
+    compact ranges ("0-15")."""
+    cpus = sorted(os.sched_getaffinity(0))
+    spans, start = [], cpus[0]
+    for a, b in zip(cpus, cpus[1:] + [None]):
+        if b != a + 1:
+            spans.append(f"{start}-{a}" if a != start else f"{a}")
+            start = b
+    return len(cpus), ",".join(spans)
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
     q, k, v = make_inputs(w, 0)
-    threads = len(os.sched_getaffinity(0))
+    threads, affinity = cpu_affinity()
     n_rows = args.ref_rows
     total_f, total_t = 0.0, 0.0
     for i in range(args.warmup + args.steps):
@@ -225,7 +237,7 @@ def run_reference(args, w, rank, world):
         "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
                    "threshold": THRESHOLD},
         "cpu_baseline": {"kind": "oracle", "value": val, "unit": "TFLOP/s", "cores": threads,
-                         "sample": sample},
+                         "affinity": affinity, "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -492,9 +504,10 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        threads = len(os.sched_getaffinity(0))
+        threads, affinity = cpu_affinity()
         f, t = oracle_sample(q, k, v, w, "mxfp8", args.cpu_rows, threads)
-        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "affinity": affinity,
+               "kind": "oracle",
                "sample": f"{args.cpu_rows} query rows of head 0 (all {Sk} keys), MXFP8, "
                          f"{t:.1f} s; rows are independent so the rate extrapolates exactly"}
 
