@@ -593,16 +593,20 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         const bool grew = t > 0 && tmax > rs.m_acc;
         const float rescale = grew ? expf((rs.m_acc - tmax) * p.sm_scale) : 1.0f;
         rs.m_acc = (t == 0) ? tmax : fmaxf(rs.m_acc, tmax);
-        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
-        if (__any_sync(0xFFFFFFFFu, grew)) {
-            ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
-            rescale_o(lane_addr, D, rescale);
-        }
+        const bool any_grew = __any_sync(0xFFFFFFFFu, grew);
         const uint32_t sb0 = efq_block(s0, bm0, rs.m_acc, p, w0);
         const uint32_t sb1 = efq_block(s1, bm1, rs.m_acc, p, w1);
         const uint32_t sb2 = efq_block(s2, bm2, rs.m_acc, p, w2);
         const uint32_t sb3 = efq_block(s3, bm3, rs.m_acc, p, w3);
         sfw = (sb0 + sb1 * p.mul8) + (sb2 + sb3 * p.mul8) * p.mul16;
+        // the running maximum grows on a large share of tiles: O and l are
+        // rescaled after the conversion, so that the wait for the previous
+        // PV product overlaps it (P buffer first, as below)
+        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if (any_grew) {
+            ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
+            rescale_o(lane_addr, D, rescale);
+        }
     } else {
         constexpr bool kE4M3 = kP == kPE4M3;
         float bmax[4] = {h_max0, h_max1, 0.0f, 0.0f}, bmin[4] = {h_min0, h_min1, 0.0f, 0.0f};
