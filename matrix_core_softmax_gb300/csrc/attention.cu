@@ -508,6 +508,46 @@ __device__ __forceinline__ void rescale_o(uint32_t lane_addr, int D, float resca
     tmem_st_wait();
 }
 
+// As rescale_o, with every chunk of O and l loaded before one wait (the
+// score registers are free by then).
+__device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float rescale) {
+    tc_fence_after();
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    uint32_t lv;
+    tmem_ld32(lane_addr + kColO, r0);
+    tmem_ld32(lane_addr + kColO + 32, r1);
+    if (D == 128) {
+        tmem_ld32(lane_addr + kColO + 64, r2);
+        tmem_ld32(lane_addr + kColO + 96, r3);
+    }
+    tmem_ld1(lane_addr + kColO + D, lv);
+    tmem_ld_wait();
+    tmem_reg_dep(r0);
+    tmem_reg_dep(r1);
+    if (D == 128) {
+        tmem_reg_dep(r2);
+        tmem_reg_dep(r3);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        r0[j] = __float_as_uint(__uint_as_float(r0[j]) * rescale);
+        r1[j] = __float_as_uint(__uint_as_float(r1[j]) * rescale);
+    }
+    tmem_st32(lane_addr + kColO, r0);
+    tmem_st32(lane_addr + kColO + 32, r1);
+    if (D == 128) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            r2[j] = __float_as_uint(__uint_as_float(r2[j]) * rescale);
+            r3[j] = __float_as_uint(__uint_as_float(r3[j]) * rescale);
+        }
+        tmem_st32(lane_addr + kColO + 64, r2);
+        tmem_st32(lane_addr + kColO + 96, r3);
+    }
+    tmem_st1(lane_addr + kColO + D, __float_as_uint(__uint_as_float(lv) * rescale));
+    tmem_st_wait();
+}
+
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
@@ -605,7 +645,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
         if (any_grew) {
             ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
-            rescale_o(lane_addr, D, rescale);
+            rescale_o_all(lane_addr, D, rescale);
         }
     } else {
         constexpr bool kE4M3 = kP == kPE4M3;
