@@ -48,7 +48,7 @@ namespace fsa {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kPBuf = 2;  // P buffers in TMEM: tile t uses t % 2 (one per warpgroup)
+constexpr int kPBuf = 2;  // P buffers in TMEM: the CTA's tile g uses g % 2 (one per warpgroup)
 constexpr int kThreads = 384;  // 2 softmax warpgroups + (K loader, MMA, V loader, spare)
 constexpr int kWarpLoad = 8, kWarpMma = 9, kWarpLoadV = 10, kWarpPv = 11;
 // Register split: launched at 168 per thread (384 x 168 = 64512), the helper
@@ -73,7 +73,7 @@ constexpr uint32_t kTmemCols = 512;
 // the same accumulator (D + 16 columns written), P0, P1 (32 each: 128 E4M3
 // bytes per row), and the scale-factor atoms (4 columns per atom)
 constexpr uint32_t kColS0 = 0, kColO = 256;  // S1 = kColS0 + 128, l = kColO + D
-constexpr uint32_t kColP = 400;              // + 32 * (t & 1)
+constexpr uint32_t kColP = 400;              // + 32 * (g & 1)
 constexpr uint32_t kColSfQ = 464, kColSfK = 468 /* +4*(g&1) */, kColSfP = 476 /* +4*(g&1) */,
                    kColSfV = 484 /* +8*(g&1): V rows 0-127, then unit scales for rows 128-255 */,
                    kColSfQ1 = 500 /* persistent kernel: scales of Q buffer 1 */;
@@ -88,7 +88,7 @@ struct __align__(1024) Smem {
     uint8_t k_sf[kStages][kAtomBytes];
     uint8_t v_sf[kStages][kAtomBytes];
     uint8_t ones_sf[kAtomBytes];
-    float tmax_x[8][128];  // row maxima of tile t in slot t % 8, read by the other warpgroup
+    float tmax_x[8][128];  // row maxima of the CTA's tile g in slot g % 8, read by the other warpgroup
     uint64_t bar_q[2];    // Q tile of buffer i landed
     uint64_t q_empty[2];  // persistent kernel: score products of the item in Q buffer i retired
     uint64_t k_full[kStages];   // K tile landed
@@ -551,7 +551,7 @@ __device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float r
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
-// then the two-stage conversion into TMEM P buffer t % 2.  A wait that gives up
+// then the two-stage conversion into TMEM P buffer g % 2.  A wait that gives up
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
