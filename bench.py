@@ -472,10 +472,13 @@ def main():
 
         def e2e_step():
             for fmt in FORMATS:
+                # the host inputs are final: consecutive calls overlap their copies
                 if cross:
-                    fsa.cross_attention_fwd_host(hq, hk, hv, fmt=fmt, threshold=THRESHOLD, out=ho)
+                    fsa.cross_attention_fwd_host(hq, hk, hv, fmt=fmt, threshold=THRESHOLD, out=ho,
+                                                 host_inputs_ready=True)
                 else:
-                    fsa.attention_fwd_host(hq, hk, hv, fmt=fmt, threshold=THRESHOLD, out=ho)
+                    fsa.attention_fwd_host(hq, hk, hv, fmt=fmt, threshold=THRESHOLD, out=ho,
+                                           host_inputs_ready=True)
 
         e2e_step()
         torch.cuda.synchronize(dev)

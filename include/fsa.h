@@ -106,6 +106,12 @@ typedef struct {
      * calibration, tau = -2.44, h = 0.61 (the pages print no values). */
     float efq_tau;
     float efq_h;
+    /* Host-buffer entry points only: nonzero declares q, k, v final when the
+     * call is made (nothing enqueued earlier on `stream` writes them), so
+     * their copy-in may start at once instead of after the work already on
+     * `stream` -- consecutive calls then overlap their copies.  0: the
+     * copies wait for that work. */
+    int host_inputs_ready;
 } fsa_options;
 
 /*

@@ -50,6 +50,7 @@ class Options(ctypes.Structure):
         ("debug_flags", ctypes.c_int),
         ("efq_tau", ctypes.c_float),
         ("efq_h", ctypes.c_float),
+        ("host_inputs_ready", ctypes.c_int),
     ]
 
 
@@ -218,12 +219,15 @@ def _host_bhsd(t, name):
 
 def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                              sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                             efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+                             efq_tau: float = 0.0, efq_h: float = 0.0, host_inputs_ready: bool = False,
+                             stream=None):
     """fsa_cross_attention_fwd_host: q, k, v contiguous HOST bf16 tensors
     ([B, H, Sq, D] and [B, H, Sk, D]; pinned memory lets the copies overlap
     the computation); returns the host output o [B, H, Sq, D] (or fills
     `out`).  Asynchronous on `stream`: synchronise it before reading o.
-    rollback_bits / rollback_count, when given, are CUDA tensors."""
+    rollback_bits / rollback_count, when given, are CUDA tensors.
+    host_inputs_ready: q, k, v are final now (no earlier work on `stream`
+    writes them), so their copy-in need not wait for that work."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _host_bhsd(t, n)
     B, H, Sq, D = q.shape
@@ -239,6 +243,7 @@ def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.host_inputs_ready = int(bool(host_inputs_ready))
     _check(load().fsa_cross_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
                                                FORMATS[fmt], float(threshold), ctypes.byref(opt),
                                                _stream(stream)), "fsa_cross_attention_fwd_host")
@@ -247,7 +252,8 @@ def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0
 
 def attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                        sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                       efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+                       efq_tau: float = 0.0, efq_h: float = 0.0, host_inputs_ready: bool = False,
+                       stream=None):
     """fsa_attention_fwd_host: self-attention on contiguous HOST bf16 tensors
     [B, H, S, D]; see cross_attention_fwd_host."""
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -264,6 +270,7 @@ def attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, o
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.host_inputs_ready = int(bool(host_inputs_ready))
     _check(load().fsa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
                                          FORMATS[fmt], float(threshold), ctypes.byref(opt),
                                          _stream(stream)), "fsa_attention_fwd_host")

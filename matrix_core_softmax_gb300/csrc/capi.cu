@@ -309,9 +309,10 @@ fsa_status host_fwd_impl(DeviceState& ds, const uint16_t* q, const uint16_t* k, 
         dv[i] = p; p += align256(kv_bytes);
         dws[i] = p;
     }
-    // everything already on the caller's stream comes first
+    // everything already on the caller's stream comes first (for the
+    // copy-in only unless the caller declared the host inputs final)
     if (cudaEventRecord(hp.start, st) != cudaSuccess ||
-        cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess ||
+        (!op.host_inputs_ready && cudaStreamWaitEvent(hp.h2d, hp.start, 0) != cudaSuccess) ||
         cudaStreamWaitEvent(hp.comp1, hp.start, 0) != cudaSuccess ||
         cudaStreamWaitEvent(hp.d2h, hp.start, 0) != cudaSuccess)
         return FSA_ERR_CUDA;

@@ -102,3 +102,21 @@ def test_host_call_rejects_device_tensors(fsa):
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError):
         fsa.attention_fwd_host(q, q, q)
+
+
+def test_host_calls_with_inputs_ready_overlap_and_stay_exact(fsa):
+    # consecutive calls whose copy-in may start before the previous call
+    # finished (host inputs declared final): every output equals the
+    # device call's, the output buffers reused call after call
+    B, H, S, D = 1, 16, 4096, 128
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=40)
+    hq, hk, hv = (_host(x, True) for x in (q, k, v))
+    outs = [torch.empty(B, H, S, D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    for i, fmt in enumerate(("mxfp8", "mxfp6", "mxfp4", "mxfp8")):
+        fsa.attention_fwd_host(hq, hk, hv, fmt=fmt, out=outs[i % 2], host_inputs_ready=True)
+        if i % 2 == 1:
+            torch.cuda.synchronize()
+            for j, f in ((i - 1, ("mxfp8", "mxfp6", "mxfp4", "mxfp8")[i - 1]), (i, fmt)):
+                ref = fsa.attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt=f)
+                assert torch.equal(outs[j % 2], ref.cpu()), (j, f)
+    assert fsa.get_device_error() == 0
