@@ -251,14 +251,16 @@ FSA_API fsa_status fsa_bf16_attention_fwd(const void *q, const void *k, const vo
  *  - Same arguments, layouts and results as fsa_attention_fwd.
  *  - Shapes whose workspace (fsa_attention_workspace_size) exceeds 64 MiB --
  *    roughly B*H*S*D above 21 million -- return FSA_ERR_INVALID_ARGUMENT.
- *  - The first call on a device looks up the array's device address with
- *    that device current (and clears a status word); make that first call
- *    before any stream capture.
+ *  - The first call on a device looks up the array's device address (and
+ *    that of a status word beside it) with that device current; make that
+ *    first call before any stream capture.
  *  - All calls on a device share the one array, which keeps the last call's
  *    contents: calls that overlap on the GPU (different streams, or several
  *    host threads) race on it and must be serialised by the caller.
- *  - A kernel whose bounded wait ran out records that in a status word of
- *    this entry point, not in the word fsa_get_device_error reads.
+ *  - A kernel whose bounded wait ran out sets the status word beside the
+ *    array (a static device object, zero at load); fsa_get_device_error
+ *    reads and clears it together with the other entry points' word and
+ *    allocates nothing, so these callers can use it too.
  */
 FSA_API fsa_status fsa_attention_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
                                              int B, int H, int S, int D, int fmt,
@@ -303,9 +305,10 @@ FSA_API fsa_status fsa_cross_attention_fwd_host(const void *q, const void *k, co
                                                 float threshold, const fsa_options *opt,
                                                 void *stream);
 
-/* Synchronises `stream`, then reads and clears the device error word of the
- * current device: FSA_OK, FSA_ERR_TIMEOUT, or FSA_ERR_CUDA if the sync
- * itself failed. */
+/* Synchronises `stream`, then reads and clears the device error words of the
+ * current device (the allocating entry points' word and, once that entry
+ * point has run there, fsa_attention_fwd_noalloc's): FSA_OK, FSA_ERR_TIMEOUT,
+ * or FSA_ERR_CUDA if the sync itself failed.  Allocates no device memory. */
 FSA_API fsa_status fsa_get_device_error(void *stream);
 
 /* Static description of a status code. */

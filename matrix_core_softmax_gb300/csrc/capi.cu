@@ -359,6 +359,10 @@ fsa_status host_fwd_impl(DeviceState& ds, const uint16_t* q, const uint16_t* k, 
     return FSA_OK;
 }
 
+// Device address of the non-allocating entry point's status word on device
+// dev, or null before that entry point was set up there.
+unsigned int* noalloc_status_word(int dev);
+
 }  // namespace
 }  // namespace fsa
 
@@ -585,16 +589,29 @@ fsa_status fsa_bf16_attention_fwd(const void* q, const void* k, const void* v, v
 
 fsa_status fsa_get_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FSA_ERR_CUDA;
-    int dev;
-    DeviceState* ds;
-    fsa_status s = current_device(&dev, &ds);
-    if (s != FSA_OK) return s;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FSA_ERR_UNSUPPORTED;
+    // two words may hold a status: the one of the allocating entry points
+    // (allocated on their first call) and the non-allocating entry point's
+    // static one (once it was set up on this device); nothing is allocated
+    // here, so a caller of the non-allocating entry point may use this too
+    unsigned int* words[2] = {nullptr, noalloc_status_word(dev)};
+    {
+        std::lock_guard<std::mutex> lk(g_dev[dev].mu);
+        words[0] = g_dev[dev].err;
+    }
     unsigned int w = 0;
-    if (cudaMemcpy(&w, ds->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FSA_ERR_CUDA;
-    if (w) {
-        const unsigned int zero = 0;
-        if (cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
-            return FSA_ERR_CUDA;
+    for (unsigned int* word : words) {
+        if (!word) continue;
+        unsigned int x = 0;
+        if (cudaMemcpy(&x, word, sizeof(x), cudaMemcpyDeviceToHost) != cudaSuccess) return FSA_ERR_CUDA;
+        if (x) {
+            const unsigned int zero = 0;
+            if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+                return FSA_ERR_CUDA;
+        }
+        w |= x;
     }
     if (w & kErrTimeout) return FSA_ERR_TIMEOUT;
     return w ? FSA_ERR_CUDA : FSA_OK;
@@ -663,14 +680,20 @@ fsa_status noalloc_setup(int dev, NoAllocDevice** out) {
             cudaGetLastError();
             return FSA_ERR_CUDA;
         }
-        // the status word must start at zero; nothing else needs clearing
-        // (every call rewrites the codes and resets the scale atoms)
-        if (cudaMemset(st, 0, sizeof(unsigned int)) != cudaSuccess) return FSA_ERR_CUDA;
+        // nothing needs clearing here: the status word is a static device
+        // object, zero when the module loads, and fsa_get_device_error
+        // clears it after reading; every call rewrites the codes and resets
+        // the scale atoms of the array
         d.ws = ws;
         d.status = static_cast<unsigned int*>(st);
     }
     *out = &d;
     return FSA_OK;
+}
+
+unsigned int* noalloc_status_word(int dev) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    return g_noalloc[dev].status;
 }
 
 }  // namespace

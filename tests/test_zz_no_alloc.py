@@ -1,11 +1,22 @@
 """The non-allocating entry point, fsa_attention_fwd_noalloc.
 
-It exists for callers that may not allocate device memory while running: it
-keeps the MX copies of Q, K, V in a fixed 64 MiB array inside the library
-instead of a cudaMalloc'ed workspace.  Called here through the C ABI, twice
-in a row on different inputs and formats, and compared with the allocating
-entry point, fsa_attention_fwd, within the parity tolerance of the other
-attention tests.  This file is collected last on purpose."""
+Some callers cannot allocate device memory while they run: a program whose
+whole device memory budget belongs to its own allocator, or a
+latency-critical loop in which a cudaMalloc/cudaFree could synchronise the
+device or fail under memory pressure.  For them this entry point keeps the
+MX copies of Q, K and V in a fixed 64 MiB array that is part of the library
+image, instead of a workspace it would have to allocate.
+
+Checked here through the C ABI: two calls in a row on different inputs and
+formats give exactly the bytes of the allocating entry point,
+fsa_attention_fwd, on the same inputs (the same kernels run on the same
+data, so the result is identical, which is well within the parity
+tolerance of the other attention tests); the device's free memory does not
+move across the two calls; the status word the kernels would set on a
+timed-out wait reads zero through fsa_get_device_error, which allocates
+nothing either; shapes beyond the array are refused.  The file is named so
+that pytest collects it last, and it works alone in a fresh process as well
+as after the other tests."""
 import ctypes
 
 import numpy as np
@@ -28,28 +39,43 @@ def fsa():
     return m
 
 
-def _noalloc(fsa, q, k, v, fmt, theta=8.0):
+def _noalloc(fsa, q, k, v, o, fmt, theta=8.0):
     B, H, S, D = q.shape
-    o = torch.empty_like(q)
     st = fsa.load().fsa_attention_fwd_noalloc(
         ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
         ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()), B, H, S, D,
-        fsa.FORMATS[fmt], ctypes.c_float(theta), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        fsa.FORMATS[fmt], ctypes.c_float(theta),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0, fsa.status_string(st)
-    return o
 
 
-def test_noalloc_matches_allocating_entry_point_on_two_calls(fsa):
-    cases = [((1, 4, 1000, 128), "mxfp8", 31), ((2, 3, 777, 64), "mxfp4", 32)]
+def test_noalloc_equals_allocating_entry_point_on_two_calls(fsa):
+    # the second case's workspace is about 37 MiB: an allocating call would
+    # show in the free memory
+    cases = [((1, 4, 1000, 128), "mxfp8", 31), ((2, 8, 6000, 128), "mxfp4", 32)]
+    inputs = []
     for (B, H, S, D), fmt, seed in cases:
         q, k, v = (to_dev(x) for x in fsa_inputs.qkv(B, H, S, D, seed=seed))
-        got = _noalloc(fsa, q, k, v, fmt)
-        torch.cuda.synchronize()
+        inputs.append((q, k, v, torch.empty_like(q), fmt))
+    # one round first: it loads the library's device code, the static array
+    # and every kernel these calls use (device code may load lazily, kernel
+    # by kernel, on first use) if nothing of it ran yet in this process
+    for q, k, v, _, fmt in inputs:
+        _noalloc(fsa, q, k, v, torch.empty_like(q), fmt)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for q, k, v, o, fmt in inputs:
+        _noalloc(fsa, q, k, v, o, fmt)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert fsa.get_device_error() == 0          # the entry point's status word, read and cleared
+    for q, k, v, o, fmt in inputs:
         ref = fsa.attention_fwd(q, k, v, fmt=fmt)
         assert fsa.get_device_error() == 0
-        a, b = to_f64(got).reshape(-1, D), to_f64(ref).reshape(-1, D)
-        assert np.all(np.isfinite(a))
-        assert oracle.rel_l2(a, b) <= TOL
+        assert torch.equal(o, ref)
+        D = q.shape[-1]
+        assert oracle.rel_l2(to_f64(o).reshape(-1, D), to_f64(ref).reshape(-1, D)) <= TOL
+        assert np.all(np.isfinite(to_f64(o)))
 
 
 def test_noalloc_rejects_shapes_beyond_its_array(fsa):
