@@ -24,6 +24,10 @@ struct HostPipe {
     cudaEvent_t in_ready[2] = {}, in_free[2] = {}, out_ready[2] = {}, out_free[2] = {};
     cudaEvent_t start = nullptr, copies_done = nullptr, comp1_done = nullptr;
     bool init = false;
+    // buffer-set layout of the last call (heads per chunk and the shape it
+    // was carved for); a call with another layout starts its copies only
+    // after all of the last call's work
+    int64_t last_G = 0, last_Sq = 0, last_Sk = 0, last_D = 0;
 };
 
 struct DeviceState {
@@ -309,6 +313,20 @@ fsa_status host_fwd_impl(DeviceState& ds, const uint16_t* q, const uint16_t* k, 
         dv[i] = p; p += align256(kv_bytes);
         dws[i] = p;
     }
+    // a different layout carves the buffer sets at other offsets, so a
+    // region this call writes may be one the last call's kernels or copies
+    // still use under another name: the copy-in (and through its events
+    // everything after it) waits for the whole last call, whose copy-outs
+    // follow all of its kernels.  With the same layout the per-set events
+    // below order every reuse.
+    const bool relayout = hp.last_G != G || hp.last_Sq != Sq || hp.last_Sk != Sk || hp.last_D != D;
+    if (relayout && (cudaStreamWaitEvent(hp.h2d, hp.copies_done, 0) != cudaSuccess ||
+                     cudaStreamWaitEvent(hp.h2d, hp.comp1_done, 0) != cudaSuccess))
+        return FSA_ERR_CUDA;
+    hp.last_G = G;
+    hp.last_Sq = Sq;
+    hp.last_Sk = Sk;
+    hp.last_D = D;
     // everything already on the caller's stream comes first (for the
     // copy-in only unless the caller declared the host inputs final)
     if (cudaEventRecord(hp.start, st) != cudaSuccess ||

@@ -9,6 +9,7 @@ import torch
 
 import fsa_inputs
 import oracle
+import parity
 from gpu_util import to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +60,7 @@ def test_host_call_matches_oracle(fsa, pinned):
     got = o.float().numpy().astype(np.float64).reshape(-1, D)
     rows = np.arange(0, B * H * S, 97)
     ref = oracle.attention(q, k, v, fmt="mxfp4", mode="fused", rows=rows)["out"]
-    assert oracle.rel_l2(got[rows], ref) <= TOL
+    parity.check_out(f"host call pinned={pinned} mxfp4", got[rows], ref)
 
 
 def test_host_call_rollback_bits_follow_the_chunks(fsa):
@@ -119,4 +120,36 @@ def test_host_calls_with_inputs_ready_overlap_and_stay_exact(fsa):
             for j, f in ((i - 1, ("mxfp8", "mxfp6", "mxfp4", "mxfp8")[i - 1]), (i, fmt)):
                 ref = fsa.attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt=f)
                 assert torch.equal(outs[j % 2], ref.cpu()), (j, f)
+    assert fsa.get_device_error() == 0
+
+
+def test_overlapping_host_calls_with_different_layouts_stay_exact(fsa):
+    # consecutive calls with the host inputs declared final, alternating
+    # between shapes whose chunk buffer sets are carved at different offsets
+    # (different Sq, Sk and heads per chunk) and between two streams: a
+    # call with a new layout must not overwrite buffers the previous call's
+    # kernels or copies still use, so every output equals the device call's
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    shapes = [(1, 16, 4096, 1000, 128), (1, 20, 2000, 3000, 128), (1, 16, 4096, 1000, 128),
+              (1, 12, 3000, 3000, 64)]
+    cases = []
+    for i, (B, H, Sq, Sk, D) in enumerate(shapes):
+        q, _, _ = fsa_inputs.qkv(B, H, Sq, D, seed=50 + i)
+        _, k, v = fsa_inputs.qkv(B, H, Sk, D, seed=60 + i)
+        cases.append((q, k, v, tuple(_host(x, True) for x in (q, k, v))))
+    # the largest layout first, so the buffers are not reallocated (and the
+    # device not synchronised) between the overlapping calls below
+    B, H, Sq, Sk, D = shapes[1]
+    fsa.cross_attention_fwd_host(*cases[1][3], fmt="mxfp8", host_inputs_ready=True)
+    torch.cuda.synchronize()
+    fmts = ("mxfp8", "mxfp4", "mxfp6", "mxfp8")
+    outs = []
+    for i, (q, k, v, h) in enumerate(cases):
+        st = s1 if i % 2 == 0 else s2
+        outs.append(fsa.cross_attention_fwd_host(*h, fmt=fmts[i], host_inputs_ready=True, stream=st))
+    torch.cuda.synchronize()
+    assert fsa.get_device_error() == 0
+    for (q, k, v, _), fmt, o in zip(cases, fmts, outs):
+        ref = fsa.cross_attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt=fmt)
+        assert torch.equal(o, ref.cpu()), fmt
     assert fsa.get_device_error() == 0
