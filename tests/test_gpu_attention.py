@@ -1,11 +1,15 @@
 """GPU parity of the fused attention (fsa_attention_fwd_ex, through the C
 ABI) and of the BF16 baseline against the CPU oracle.
 
-Bar: output relative L2 <= 5e-3 against the oracle's FP64 result for the
-fused kernel (1e-2 against exact attention for the BF16 kernel); rollback
-decisions identical per (row, tile) except near-ties, i.e. tiles whose gate
-margin |max s - m - theta| is below 1e-4 in score units, where FP32
-accumulation order on the GPU may legitimately decide the other way."""
+Bar (tests/parity.py): output relative L2 <= 5e-3 against the oracle's
+FP64 result for the fused kernel over the compared rows, every row within
+0.1 and at most 1 % of them above 5e-3 (1e-2 against exact attention for
+the BF16 kernel); rollback decisions identical
+per (row, tile) except near-ties, i.e. tiles whose gate margin |max s - m -
+theta| is below 1e-4 in score units, where FP32 accumulation order on the
+GPU may legitimately decide the other way -- counted, and at most 0.1 % of
+the decisions.  The full-size workloads the bench measures are in
+test_gpu_configs.py."""
 import math
 
 import numpy as np
@@ -14,11 +18,11 @@ import torch
 
 import fsa_inputs
 import oracle
+import parity
 from gpu_util import to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
-TOL = 5e-3
-NEAR_TIE = 1e-4
+TOL = parity.TOL
 
 
 @pytest.fixture(scope="module")
@@ -50,11 +54,11 @@ SMALL = [(1, 2, 512, 64), (1, 1, 1, 64), (1, 2, 31, 128), (2, 1, 33, 64), (1, 1,
 def test_fused_matches_oracle_small(fsa, fmt, shape):
     B, H, S, D = shape
     q, k, v = fsa_inputs.qkv(B, H, S, D, seed=S + D)
-    o, _, _ = _run(fsa, q, k, v, fmt)
+    o, rb, _ = _run(fsa, q, k, v, fmt, want_bits=True)
     got = to_f64(o).reshape(-1, D)
-    ref = oracle.attention(q, k, v, fmt=fmt, mode="fused")["out"]
-    assert np.all(np.isfinite(got))
-    assert oracle.rel_l2(got, ref) <= TOL
+    r = oracle.attention(q, k, v, fmt=fmt, mode="fused", want_bits=True, want_margins=True)
+    skip, _ = parity.check_bits(f"small {shape} {fmt} bits", rb.cpu().numpy(), r["bits"], r["margins"])
+    parity.check_out(f"small {shape} {fmt}", got, r["out"], skip_rows=skip)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp6", "mxfp4"])
@@ -64,12 +68,10 @@ def test_rollback_decisions_match_oracle(fsa, fmt):
     o, rb, cnt = _run(fsa, q, k, v, fmt, want_bits=True)
     r = oracle.attention(q, k, v, fmt=fmt, mode="fused", want_bits=True, want_margins=True)
     bits = rb.cpu().numpy()
-    assert set(np.unique(bits)) <= {0, 1}
-    near = np.abs(np.nan_to_num(r["margins"], nan=1.0)) < NEAR_TIE
+    skip, _ = parity.check_bits(f"stress h2 s4096 {fmt} bits", bits, r["bits"], r["margins"])
     assert r["rollback_count"] > 0
-    assert np.array_equal(bits[~near], r["bits"][~near])
     assert cnt == int(bits.sum())
-    assert oracle.rel_l2(to_f64(o).reshape(-1, D), r["out"]) <= TOL
+    parity.check_out(f"stress h2 s4096 {fmt}", to_f64(o).reshape(-1, D), r["out"], skip_rows=skip)
 
 
 def _sample(BH, S, per_head=96, seed=0):
@@ -92,35 +94,8 @@ def test_fused_full_size_h16_s8192(fsa, fmt):
     assert np.all(np.isfinite(got))
     rows = _sample(B * H, S)
     ref = oracle.attention(q, k, v, fmt=fmt, mode="fused", rows=rows)
-    assert oracle.rel_l2(got[rows], ref["out"]) <= TOL
+    parity.check_out(f"h16-s8192 seed 0 {fmt}", got[rows], ref["out"])
     assert cnt == 0          # N(0,1) inputs never pass the frozen reference by 8
-
-
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
-def test_fused_full_size_rollback_stress(fsa, fmt):
-    B, H, S, D = 1, 8, 32768, 128
-    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=0, stress_from=16384)
-    o, rb, cnt = _run(fsa, q, k, v, fmt, want_bits=True)
-    rows = _sample(B * H, S, per_head=48)
-    r = oracle.attention(q, k, v, fmt=fmt, mode="fused", rows=rows, want_bits=True,
-                         want_margins=True)
-    bits = rb.cpu().numpy()[rows]
-    near = np.abs(np.nan_to_num(r["margins"], nan=1.0)) < NEAR_TIE
-    assert np.array_equal(bits[~near], r["bits"][~near])
-    assert cnt > 0
-    assert oracle.rel_l2(to_f64(o).reshape(-1, D)[rows], r["out"]) <= TOL
-
-
-def test_fused_video_dit_shape_sampled(fsa):
-    B, H, S, D = 1, 40, 75600, 128
-    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=0)
-    o, _, _ = _run(fsa, q, k, v, "mxfp8")
-    rows = _sample(B * H, S, per_head=32)
-    rows = rows[(rows // S == 0) | (rows // S == B * H - 1)]   # two heads keep the oracle quick
-    got = to_f64(o).reshape(-1, D)[rows]
-    ref = oracle.attention(q, k, v, fmt="mxfp8", mode="fused", rows=rows)["out"]
-    assert np.all(np.isfinite(got))
-    assert oracle.rel_l2(got, ref) <= TOL
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 512, 64), (1, 1, 300, 128), (2, 2, 1000, 128), (1, 1, 5, 64)])
@@ -146,7 +121,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(fsa):
     o = fsa.attention_fwd(tq, tk, tv, fmt="mxfp8")
     assert fsa.get_device_error() == 0
     ref = oracle.attention(q, k, v, fmt="mxfp8", mode="fused")["out"]
-    assert oracle.rel_l2(to_f64(o).reshape(-1, D), ref) <= TOL
+    parity.check_out("after timeout", to_f64(o).reshape(-1, D), ref)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp6", "mxfp4"])
@@ -159,9 +134,7 @@ def test_fused_wide_and_narrow_score_ranges(fsa, fmt, qscale):
     q = fsa_inputs.to_bf16_bits(fsa_inputs.bf16_bits_to_f32(q) * np.float32(qscale))
     o, _, _ = _run(fsa, q, k, v, fmt, theta=80.0)
     ref = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=80.0)["out"]
-    got = to_f64(o).reshape(-1, D)
-    assert np.all(np.isfinite(got))
-    assert oracle.rel_l2(got, ref) <= TOL
+    parity.check_out(f"q x {qscale} {fmt}", to_f64(o).reshape(-1, D), ref)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
@@ -172,8 +145,7 @@ def test_gate_at_theta_zero(fsa, fmt):
     o, rb, cnt = _run(fsa, q, k, v, fmt, theta=0.0, want_bits=True)
     r = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=0.0, want_bits=True,
                          want_margins=True)
-    bits = rb.cpu().numpy()
-    near = np.abs(np.nan_to_num(r["margins"], nan=1.0)) < NEAR_TIE
+    skip, _ = parity.check_bits(f"theta 0 {fmt} bits", rb.cpu().numpy(), r["bits"], r["margins"])
     assert r["rollback_count"] > 100
-    assert np.array_equal(bits[~near], r["bits"][~near])
-    assert oracle.rel_l2(to_f64(o).reshape(-1, D), r["out"]) <= TOL
+    assert cnt == int(rb.sum().item())
+    parity.check_out(f"theta 0 {fmt}", to_f64(o).reshape(-1, D), r["out"], skip_rows=skip)
