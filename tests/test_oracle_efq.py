@@ -109,3 +109,48 @@ def test_calibration_is_a_local_optimum():
 def test_library_defaults_match_calibration():
     g = _golden()
     assert (g["tau"], g["h"]) == (oracle.EFQ_TAU, oracle.EFQ_H)
+
+
+def _grid_row(dot):
+    """A key row of 32 elements, every one on the E2M1 grid at scale 1 with
+    a 6 among them (so the row's MX block has scale 2^0 and is exact), whose
+    elements sum to `dot` (a multiple of 0.5).  Input construction only."""
+    mags = [6.0, 4.0, 3.0, 2.0, 1.5, 1.0, 0.5]
+    row, rest = [6.0], dot - 6.0
+    while rest != 0.0:
+        m = next(x for x in mags if x <= abs(rest))
+        row.append(math.copysign(m, rest))
+        rest -= math.copysign(m, rest)
+    assert len(row) <= 32
+    return row + [0.0] * (32 - len(row))
+
+
+def test_code_mapping_hand_computed():
+    """The code rule of the EFQ page's "Code mapping" step, code =
+    clip(floor((r - tau) / h), 0, 7) with r = u - X, checked on a block whose
+    residuals straddle chosen thresholds, the codes worked out by hand.
+
+    One query row of 32 ones and 32 keys whose dot products with it are the
+    values in DOTS (exact in MXFP4: q is 4 x 2^-2 everywhere, every key row is
+    on the E2M1 grid at scale 1); sm = ln(2) / 16, so u_j = (s_j - m) log2(e)
+    = (dot_j - 18) / 16 with m the largest score (dot 18).  The block's scale
+    exponent is X = ceil(0 - log2 6) = -2, so r = u + 2, and with tau = -2,
+    h = 0.5: code = clip(floor(2 u + 8), 0, 7) = clip(floor((dot - 18) / 8 +
+    8), 0, 7).  Each pair in DOTS sits half a unit of dot on either side of a
+    threshold (a wrong rounding, sign of tau, scale of h, offset of X or clip
+    moves at least one code).  V is one-hot (V_j = e_j, exact in MXFP4), so
+    output column j is p^_j / sum(p^) and o_j / o_0 = E2M1(code_j) / 6."""
+    DOTS = [18, 10.5, 9.5, 2.5, 1.5, -5.5, -6.5, -13.5, -14.5, -21.5, -22.5, -29.5, -30.5,
+            -37.5, -38.5, -60, 14, 6, -2, -10, -18, -26, -34, -42, -100, 17.5, 0, 4, 12, -16,
+            -24, -32]
+    CODES = [7, 7, 6, 6, 5, 5, 4, 4, 3, 3, 2, 2, 1, 1, 0, 0, 7, 6, 5, 4, 3, 2, 1, 0, 0, 7, 5,
+             6, 7, 3, 2, 1]
+    E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    q = fsa_inputs.to_bf16_bits(np.ones((1, 1, 1, 32), np.float32))
+    k = fsa_inputs.to_bf16_bits(np.array([_grid_row(d) for d in DOTS], np.float32)[None, None])
+    v = fsa_inputs.to_bf16_bits(np.eye(32, dtype=np.float32)[None, None])
+    o = oracle.attention(q, k, v, fmt="mxfp4", mode="efq", sm_scale=math.log(2.0) / 16.0,
+                         efq_tau=-2.0, efq_h=0.5)["out"][0]
+    ratios = o / o[0]
+    expected = np.array([E2M1[c] / 6.0 for c in CODES])
+    assert np.max(np.abs(ratios - expected)) < 1e-12, list(zip(DOTS, ratios * 6.0, CODES))
