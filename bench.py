@@ -13,6 +13,13 @@ the device with the copies overlapping the computation.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
   python bench.py --schedule    # 20-step hybrid MXFP6/MXFP4 schedule vs all-BF16 / all-MXFP4
+  python bench.py --mma-peaks   # only the tensor-core rate probe
+
+After the timed region the default run also times the task's other
+workloads (`configs`: B=1 H=16 S=8192, the rollback-stress shape, the
+B=1 H=32 sequence sweep with the BF16 kernel) and measures the dense
+block-scaled MMA rates with the library's tensor-core rate probe
+(`mma_peaks`), which are the roofline denominators of every fraction.
 """
 from __future__ import annotations
 
@@ -83,9 +90,13 @@ def make_inputs(w, seed):
     return q, k, v
 
 
-def peaks():
-    """Measured peaks; the MX rate is the measured bf16 rate times the nominal
-    fp8/bf16 ratio (4.5 / 2.25)."""
+def peaks(mma=None):
+    """Roofline denominators (TFLOP/s, GB/s).  bf16 and HBM: the driver's
+    measurement (MEASURED_PEAKS.json: cuBLAS GEMM, copy).  Block-scaled MMA
+    rates: the tensor-core rate probe of this run (measure_mma_peaks) when
+    given -- R8 (E4M3), R6 (E2M3), R4 (packed E2M1, kind::mxf4) and the
+    attention kernel's own product mix -- else the bf16 rate times the
+    nominal ratios (fp8 4.5 / bf16 2.25, fp4 13.5 / 2.25)."""
     p = {"source": "fallback", "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -95,11 +106,84 @@ def peaks():
              "hbm_gbs": float(m["hbm_gbs"])}
     except (OSError, KeyError, ValueError):
         pass
-    ratio = 4.5 / 2.25
-    p["mx8_burst"] = p["bf16_burst"] * ratio
-    p["mx8_sustained"] = p["bf16_sustained"] * ratio
-    p["fp4_sustained"] = p["bf16_sustained"] * (13.5 / 2.25)
+    if mma:
+        p["mx_source"] = "measured by the tensor-core rate probe in this run"
+        p["mx8_burst"] = mma["mxf8f6f4_e4m3"]["burst_tflops"]
+        p["mx8_sustained"] = mma["mxf8f6f4_e4m3"]["sustained_tflops"]
+        p["mx6_sustained"] = mma["mxf8f6f4_e2m3"]["sustained_tflops"]
+        p["fp4_sustained"] = mma["mxf4_e2m1"]["sustained_tflops"]
+        p["attn_tile_sustained"] = mma["attention_tile_e4m3"]["sustained_tflops"]
+    else:
+        p["mx_source"] = f"{p['source']} bf16 rate x nominal ratios"
+        ratio = 4.5 / 2.25
+        p["mx8_burst"] = p["bf16_burst"] * ratio
+        p["mx8_sustained"] = p["bf16_sustained"] * ratio
+        p["mx6_sustained"] = p["mx8_sustained"]
+        p["fp4_sustained"] = p["bf16_sustained"] * (13.5 / 2.25)
+        p["attn_tile_sustained"] = None
     return p
+
+
+def format_roofline(pk, fmt):
+    """Dense block-scaled MMA roofline of a format: both products at the
+    rate of its element type -- E4M3 (MXFP8), E2M3 (MXFP6); for MXFP4 the
+    score product at the four-bit rate and the PV product on six-bit P, so
+    2 / (1/R4 + 1/R6)."""
+    if fmt == "mxfp8":
+        return pk["mx8_sustained"]
+    if fmt == "mxfp6":
+        return pk["mx6_sustained"]
+    return 2.0 / (1.0 / pk["fp4_sustained"] + 1.0 / pk["mx6_sustained"])
+
+
+# tensor-core rate probes (fsa_mma_rate_probe), in the order they are measured
+PROBES = ("mxf8f6f4_e4m3", "mxf8f6f4_e2m3", "mxf4_e2m1", "attention_tile_e4m3", "f16_bf16")
+
+
+def measure_mma_peaks(fsa, dev, stream, n_sm, sustained_s=2.0, launch_s=0.02):
+    """Measured tensor-core rates on this GPU (TFLOP/s): for every probe kind
+    one CTA per SM issues its products back to back.  burst = the best of
+    three single launches of about launch_s; sustained = back-to-back
+    launches for about sustained_s, timed as a whole, with the SM clocks
+    sampled meanwhile (the tensor core at full rate runs into the power cap,
+    as a long attention step does)."""
+    out = {}
+    for kind in PROBES:
+        it0 = 512
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fsa.mma_rate_probe(kind, n_sm, it0)          # warm-up (loads the kernel)
+        e0.record(stream)
+        fsa.mma_rate_probe(kind, n_sm, it0)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t0 = e0.elapsed_time(e1) / 1e3
+        iters = max(it0, int(it0 * launch_s / max(t0, 1e-6)))
+        best = 0.0
+        for _ in range(3):
+            e0.record(stream)
+            fl = fsa.mma_rate_probe(kind, n_sm, iters)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            best = max(best, fl / (e0.elapsed_time(e1) / 1e3) / 1e12)
+        n = max(3, int(sustained_s / launch_s))
+        with ClockSampler(int(dev.index or 0)) as clk:
+            e0.record(stream)
+            tot = 0.0
+            for _ in range(n):
+                tot += fsa.mma_rate_probe(kind, n_sm, iters)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        sus = tot / (e0.elapsed_time(e1) / 1e3) / 1e12
+        c = clk.summary()
+        out[kind] = {"burst_tflops": best, "sustained_tflops": sus, "sm_mhz": c["sm_mhz"],
+                     "reasons": c["reasons"]}
+        if c["sm_mhz"]:
+            # flops per SM per clock at the sustained rate
+            out[kind]["flops_per_sm_clk"] = sus * 1e12 / (n_sm * c["sm_mhz"] * 1e6)
+    st = fsa.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error in the MMA rate probe: {fsa.status_string(st)}")
+    return out
 
 
 def traffic_from_profiles():
@@ -210,6 +294,114 @@ def cpu_affinity():
     return len(cpus), ",".join(spans)
 
 
+CONFIG_FORMATS = ("mxfp8", "mxfp6", "mxfp4", "mxfp4_efq")
+SWEEP_S = (16384, 32768, 65536, 131072)
+
+
+def run_configs(fsa, dev, stream, seed):
+    """The task's other throughput workloads, one warm-up and one timed call
+    per format (quantizer and fused kernel timed apart, CUDA events on the
+    launching stream): B=1 H=16 S=8192 D=128; the rollback-stress shape
+    (B=1 H=8 S=32768 D=128, 1 % of the keys after 16384 scaled by 8; firings
+    counted); and the sequence sweep B=1 H=32 D=128, S in SWEEP_S, every
+    format plus the in-house BF16 kernel.  Inputs: N(0,1) drawn on the device
+    by torch's generator (seed 1234 + seed), rounded to bf16 -- the
+    distribution of the parity inputs, drawn where they are used; the shapes
+    share one buffer of the largest (H=32, S=131072: 1.07 GB per tensor,
+    larger than L2), each taking its leading elements."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + seed)
+    n_max = 32 * max(SWEEP_S) * 128
+    base = [torch.randn(n_max, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            for _ in range(3)]
+
+    def view(B, H, S, D):
+        return [t[:B * H * S * D].view(B, H, S, D) for t in base]
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def timed(fn_prep, fn_run):
+        for rep in range(2):                 # one warm-up, one timed
+            ev[0].record(stream)
+            fn_prep()
+            ev[1].record(stream)
+            fn_run()
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+        return ev[0].elapsed_time(ev[1]) / 1e3, ev[1].elapsed_time(ev[2]) / 1e3
+
+    def one(name, B, H, S, D, qkv, with_bf16, count=False):
+        F = 4.0 * B * H * S * S * D
+        o = torch.empty_like(qkv[0])
+        ws = fsa.new_workspace(B, H, S, D, device=dev)
+        r = {}
+        for fmt in CONFIG_FORMATS:
+            cnt = torch.zeros(1, dtype=torch.int64, device=dev) if count else None
+
+            def run():
+                if cnt is not None:
+                    cnt.zero_()
+                fsa.attention_run(ws, o, fmt, THRESHOLD, rollback_count=cnt)
+            tq, ta = timed(lambda: fsa.attention_prepare(*qkv, ws, fmt), run)
+            r[fmt] = {"attention_ms": 1e3 * ta, "quantize_ms": 1e3 * tq,
+                      "attention_tflops": F / ta / 1e12}
+            if cnt is not None and fmt != "mxfp4_efq":
+                r[fmt]["rollback_count"] = int(cnt.item())
+        if with_bf16:
+            _, tb = timed(lambda: None, lambda: fsa.bf16_attention_fwd(*qkv, out=o))
+            r["bf16"] = {"attention_ms": 1e3 * tb, "attention_tflops": F / tb / 1e12}
+            for fmt in CONFIG_FORMATS:
+                r[fmt]["speedup_vs_bf16_kernel"] = tb / (r[fmt]["attention_ms"] / 1e3)
+        st = fsa.get_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error in {name}: {fsa.status_string(st)}")
+        del ws, o
+        return r
+
+    out = {}
+    out["h16-s8192 B=1 H=16 S=8192 D=128"] = one("h16-s8192", 1, 16, 8192, 128,
+                                                  view(1, 16, 8192, 128), True)
+    q, k, v = view(1, 8, 32768, 128)
+    k = k.clone()
+    mask = torch.rand((1, 8, 32768), generator=g, device=dev) < 0.01
+    mask[:, :, :16384] = False
+    k[mask] = k[mask] * 8
+    out["rollback-stress B=1 H=8 S=32768 D=128 (1 % of keys after 16384 x 8)"] = one(
+        "rollback-stress", 1, 8, 32768, 128, (q, k, v), True, count=True)
+    del q, k, v, mask
+    sweep = {}
+    for S in SWEEP_S:
+        sweep[str(S)] = one(f"sweep S={S}", 1, 32, S, 128, view(1, 32, S, 128), True)
+    out["sweep B=1 H=32 D=128 (S)"] = sweep
+    del base
+    torch.cuda.empty_cache()
+    return out
+
+
+def add_config_fracs(configs, pk):
+    """Each format's attention rate as a fraction of its roofline."""
+    def walk(d):
+        for key, val in d.items():
+            if key in CONFIG_FORMATS and isinstance(val, dict):
+                fmt = "mxfp4" if key == "mxfp4_efq" else key
+                val["frac_of_format_roofline"] = val["attention_tflops"] / format_roofline(pk, fmt)
+                val["frac_of_mx8_peak"] = val["attention_tflops"] / pk["mx8_sustained"]
+            elif isinstance(val, dict):
+                walk(val)
+    walk(configs)
+
+
+def bench_config(args, w):
+    """The `config` object of both arms' JSON lines."""
+    B, H, S, D = w["B"], w["H"], w["S"], w["D"]
+    Sk = keys(w)
+    return {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
+            "threshold": THRESHOLD, "non_causal": True,
+            "l2": (f"inputs {2 * B * H * S * D / 1e6:.0f} MB (Q), "
+                   f"{2 * B * H * Sk * D / 1e6:.0f} MB (K, V) each"),
+            "step": "per format: quantize Q,K,V + fused attention"}
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
@@ -234,8 +426,7 @@ def run_reference(args, w, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic N(0,1) bf16, seed 0",
-        "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
-                   "threshold": THRESHOLD},
+        "config": bench_config(args, w),
         "cpu_baseline": {"kind": "oracle", "value": val, "unit": "TFLOP/s", "cores": threads,
                          "affinity": affinity, "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -306,6 +497,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-efq", action="store_true", help="skip the EFQ-Softmax format")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (h16-s8192, rollback stress, the S sweep)")
+    ap.add_argument("--no-mma-probe", action="store_true",
+                    help="skip the tensor-core rate probe (peaks from the bf16 rate x nominal ratios)")
+    ap.add_argument("--mma-peaks", action="store_true",
+                    help="only measure the tensor-core rates and print them")
     ap.add_argument("--cpu-rows", type=int, default=12288)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--schedule", action="store_true",
@@ -334,6 +531,14 @@ def main():
         dist.barrier()
         fsa_build.build()
     fsa.load()
+    if args.mma_peaks:
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        res = measure_mma_peaks(fsa, dev, torch.cuda.current_stream(dev), n_sm)
+        if rank == 0:
+            print(json.dumps({"mma_peaks": res, "n_sm": n_sm,
+                              "probe": "fsa_mma_rate_probe, one CTA per SM, operands resident"}),
+                  flush=True)
+        return
 
     B, H, S, D = w["B"], w["H"], w["S"], w["D"]
     Sk, cross = keys(w), is_cross(w)
@@ -395,7 +600,6 @@ def main():
         elapsed = max_over_ranks(elapsed, pg, dev)
     n_calls = args.steps * len(FORMATS)
     value = aggregate_tflops(world, F, n_calls, elapsed)
-    pk = peaks()
 
     per_format = {}
     for i, fmt in enumerate(FORMATS):
@@ -408,7 +612,6 @@ def main():
             "quantize_ms": 1e3 * kq,
             "attention_tflops": F / ka / 1e12,
             "with_quantize_tflops": F / (ka + kq) / 1e12,
-            "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
             "quantize_gbs": (B * H * (S + 2 * Sk) * D * (2 + 1 + 1 / 32)) / kq / 1e9,
         }
     # the EFQ-Softmax producer (MXFP4 Q/K/V, E2M1 P from the shifted scores,
@@ -435,14 +638,10 @@ def main():
                 t_a.append(ev[1].elapsed_time(ev[2]) / 1e3)
         ka = statistics.mean(t_a)
         efq = {"attention_kernel_ms": 1e3 * ka, "quantize_ms": 1e3 * statistics.mean(t_q),
-               "attention_tflops": F / ka / 1e12, "frac_of_mx_mma_peak": F / ka / 1e12 / pk["mx8_sustained"],
+               "attention_tflops": F / ka / 1e12,
                "note": "EFQ-Softmax producer: MXFP4 Q/K/V, running row maximum, E2M1 P"}
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error in the EFQ format")
-
-    per_format["mxfp4"]["frac_of_fp4_qk_roofline"] = (
-        per_format["mxfp4"]["attention_tflops"] /
-        (2.0 / (1.0 / pk["fp4_sustained"] + 1.0 / pk["mx8_sustained"])))
 
     # in-house BF16 flash-attention baseline, same inputs
     bf16 = None
@@ -457,8 +656,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize(dev)
         tb = e0.elapsed_time(e1) / 1e3 / nb
-        bf16 = {"kernel_ms": 1e3 * tb, "tflops": F / tb / 1e12,
-                "frac_of_bf16_peak": F / tb / 1e12 / pk["bf16_sustained"]}
+        bf16 = {"kernel_ms": 1e3 * tb, "tflops": F / tb / 1e12}
         for fmt in FORMATS:
             per_format[fmt]["speedup_vs_bf16_kernel"] = tb / (per_format[fmt]["attention_kernel_ms"] / 1e3)
 
@@ -502,6 +700,30 @@ def main():
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error during e2e")
 
+    # the other workloads of the task's list, then the tensor-core rate probe
+    # (last: it runs the GPU into its power cap)
+    configs = None
+    if not args.no_configs and not cross:
+        configs = run_configs(fsa, dev, stream, rank)
+    mma = None
+    if not args.no_mma_probe:
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        mma = measure_mma_peaks(fsa, dev, stream, n_sm)
+    pk = peaks(mma)
+    for fmt in FORMATS:
+        pf = per_format[fmt]
+        pf["frac_of_mx_mma_peak"] = pf["attention_tflops"] / pk["mx8_sustained"]
+        pf["frac_of_format_roofline"] = pf["attention_tflops"] / format_roofline(pk, fmt)
+        if pk["attn_tile_sustained"]:
+            pf["frac_of_attention_tile_mma_rate"] = pf["attention_tflops"] / pk["attn_tile_sustained"]
+    if efq:
+        efq["frac_of_mx_mma_peak"] = efq["attention_tflops"] / pk["mx8_sustained"]
+        efq["frac_of_format_roofline"] = efq["attention_tflops"] / format_roofline(pk, "mxfp4")
+    if bf16:
+        bf16["frac_of_bf16_peak"] = bf16["tflops"] / pk["bf16_sustained"]
+    if configs:
+        add_config_fracs(configs, pk)
+
     if rank != 0:
         return
 
@@ -518,9 +740,9 @@ def main():
     roof = {"bound": "tensor", "kernel": "fsa_attn_fwd_kernel (MXFP8)",
             "achieved": a8["attention_tflops"], "peak": pk["mx8_sustained"], "unit": "TFLOP/s",
             "frac": a8["attention_tflops"] / pk["mx8_sustained"],
-            "peak_note": (f"{pk['source']} bf16 sustained {pk['bf16_sustained']:.1f} TFLOP/s x 2 "
-                          "(nominal fp8/bf16 ratio); burst-based peak "
-                          f"{pk['mx8_burst']:.1f}"),
+            "peak_note": (f"dense E4M3 block-scaled MMA (kind::mxf8f6f4) rate, {pk['mx_source']}: "
+                          f"sustained {pk['mx8_sustained']:.1f}, burst {pk['mx8_burst']:.1f} TFLOP/s; "
+                          "one CTA per SM issuing M=128 N=256 K=32 products back to back"),
             "algorithmic_flops_per_launch": F,
             # DRAM counters exist for the default workload's kernel only
             "traffic": traffic_from_profiles() if args.workload == "video-dit" else None}
@@ -530,17 +752,15 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mx (e4m3|e2m3|e2m1 x e8m0) mma, fp32 accumulate",
         "data": "synthetic N(0,1) bf16, seed = rank",
-        "config": {"workload": workload_name(args.workload, w), "formats": list(FORMATS),
-                   "threshold": THRESHOLD, "non_causal": True,
-                   "l2": (f"inputs {2 * B * H * S * D / 1e6:.0f} MB (Q), "
-                          f"{2 * B * H * Sk * D / 1e6:.0f} MB (K, V) each"),
-                   "step": "per format: quantize Q,K,V + fused attention"},
+        "config": bench_config(args, w),
         "per_format": per_format,
         "bf16_baseline": bf16,
         "efq_format": efq,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "mma_peaks": mma,
+        "configs": configs,
         "gpu_launches": args.steps * len(FORMATS) * 4,
         "clocks": clk.summary(),
     }

@@ -305,6 +305,36 @@ FSA_API fsa_status fsa_cross_attention_fwd_host(const void *q, const void *k, co
                                                 float threshold, const fsa_options *opt,
                                                 void *stream);
 
+/*
+ * fsa_mma_rate_probe -- the tensor-core rate the fused kernel is measured
+ * against.  (A measurement aid of this library, not part of the method; the
+ * pages compare their kernels' speed only with BF16 attention, "Fused-Softmax
+ * shifts ...", paragraph 8, and print no peak.)
+ *
+ * Launches `ctas` CTAs (one per SM: pass the SM count) that each issue
+ * `iters` groups of tensor-core products back to back, with operands of
+ * pseudo-random finite values already in shared memory and tensor memory and
+ * nothing else to do, on `stream`; the caller times the launch.
+ *  kind 0: kind::mxf8f6f4 block-scaled MMA, E4M3 x E4M3, M = 128, N = 256,
+ *          four K = 32 instructions per group;
+ *  kind 1: the same with E2M3 x E2M3 (six-bit) operands;
+ *  kind 2: kind::mxf4, packed E2M1 x E2M1, M = 128, N = 256, four K = 64
+ *          instructions per group (two E8M0 scales per row and instruction);
+ *  kind 3: the fused attention kernel's products of one KV tile: the score
+ *          product (M = N = 128, K = 128, E4M3, operands in shared memory)
+ *          and the PV product (M = 128, N = 144 = D + 16, K = 128, A from
+ *          tensor memory);
+ *  kind 4: kind::f16 BF16 x BF16, M = 128, N = 256, four K = 16 instructions.
+ * *flops_per_launch (host, may be NULL) receives the launch's floating-point
+ * operations: 2 M N K per instruction; kind 3 the attention metric's
+ * 4 * 128 * 128 * 128 per group (the 16 row-sum columns not counted).
+ * Returns FSA_ERR_INVALID_ARGUMENT for kind outside 0..4, ctas outside
+ * 1..65535 or iters outside 1..2^24.  A bounded wait that ran out is reported
+ * by fsa_get_device_error.
+ */
+FSA_API fsa_status fsa_mma_rate_probe(int kind, int ctas, int iters, double *flops_per_launch,
+                                      void *stream);
+
 /* Synchronises `stream`, then reads and clears the device error words of the
  * current device (the allocating entry points' word and, once that entry
  * point has run there, fsa_attention_fwd_noalloc's): FSA_OK, FSA_ERR_TIMEOUT,

@@ -30,7 +30,7 @@ EXPORTS = ("fsa_quantize_mx", "fsa_attention_fwd", "fsa_attention_fwd_ex",
            "fsa_status_string", "fsa_release_workspace", "fsa_attention_fwd_noalloc",
            "fsa_cross_attention_fwd", "fsa_cross_attention_workspace_size",
            "fsa_cross_attention_prepare", "fsa_cross_attention_run",
-           "fsa_attention_fwd_host", "fsa_cross_attention_fwd_host")
+           "fsa_attention_fwd_host", "fsa_cross_attention_fwd_host", "fsa_mma_rate_probe")
 
 
 class FsaError(RuntimeError):
@@ -103,6 +103,8 @@ def load(path: str | None = None):
             lib.fsa_attention_fwd_noalloc.restype = I
             lib.fsa_bf16_attention_fwd.argtypes = [V, V, V, V, I, I, I, I, V]
             lib.fsa_bf16_attention_fwd.restype = I
+            lib.fsa_mma_rate_probe.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_double), V]
+            lib.fsa_mma_rate_probe.restype = I
             lib.fsa_get_device_error.argtypes = [V]
             lib.fsa_get_device_error.restype = I
             lib.fsa_status_string.argtypes = [I]
@@ -373,6 +375,20 @@ def bf16_attention_fwd(q, k, v, *, out=None, stream=None):
     _check(load().fsa_bf16_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
                                          _stream(stream)), "fsa_bf16_attention_fwd")
     return o
+
+
+# kinds of fsa_mma_rate_probe
+PROBE_KINDS = {"mxf8f6f4_e4m3": 0, "mxf8f6f4_e2m3": 1, "mxf4_e2m1": 2, "attention_tile_e4m3": 3,
+               "f16_bf16": 4}
+
+
+def mma_rate_probe(kind: str, ctas: int, iters: int, stream=None) -> float:
+    """fsa_mma_rate_probe: launches the tensor-core rate probe on the stream
+    (the caller times it) and returns the launch's floating-point operations."""
+    fl = ctypes.c_double(0.0)
+    _check(load().fsa_mma_rate_probe(PROBE_KINDS[kind], int(ctas), int(iters), ctypes.byref(fl),
+                                     _stream(stream)), "fsa_mma_rate_probe")
+    return fl.value
 
 
 def get_device_error(stream=None) -> int:

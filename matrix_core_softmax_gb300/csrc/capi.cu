@@ -605,6 +605,21 @@ fsa_status fsa_bf16_attention_fwd(const void* q, const void* k, const void* v, v
                : FSA_ERR_CUDA;
 }
 
+fsa_status fsa_mma_rate_probe(int kind, int ctas, int iters, double* flops_per_launch,
+                              void* stream) {
+    if (kind < 0 || kind > 4 || ctas < 1 || ctas > 65535 || iters < 1 || iters > (1 << 24))
+        return FSA_ERR_INVALID_ARGUMENT;
+    int dev;
+    DeviceState* ds;
+    fsa_status s = current_device(&dev, &ds);
+    if (s != FSA_OK) return s;
+    if (flops_per_launch) *flops_per_launch = mma_probe_flops(kind, ctas, iters);
+    return launch_mma_probe(kind, ctas, iters, 2000ull * 1000000ull, ds->err,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FSA_OK
+               : FSA_ERR_CUDA;
+}
+
 fsa_status fsa_get_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FSA_ERR_CUDA;
     int dev = 0;

@@ -82,6 +82,11 @@ struct Bf16Launch {
 };
 cudaError_t launch_bf16_attention(const Bf16Launch& a, cudaStream_t st);
 
+// Tensor-core rate probe (mma_rate.cu).
+double mma_probe_flops(int kind, int ctas, int iters);
+cudaError_t launch_mma_probe(int kind, int ctas, int iters, uint64_t timeout_ns,
+                             unsigned int* err_word, cudaStream_t st);
+
 // Device error word codes.
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrMisaligned = 2u;  // shared-memory base not 1024-byte aligned
