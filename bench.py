@@ -330,23 +330,27 @@ def run_configs(fsa, dev, stream, seed):
             torch.cuda.synchronize(dev)
         return ev[0].elapsed_time(ev[1]) / 1e3, ev[1].elapsed_time(ev[2]) / 1e3
 
-    def one(name, B, H, S, D, qkv, with_bf16, count=False):
+    def one(name, B, H, S, D, qkv, with_bf16, count=False, shortcut=False):
         F = 4.0 * B * H * S * S * D
         o = torch.empty_like(qkv[0])
         ws = fsa.new_workspace(B, H, S, D, device=dev)
         r = {}
-        for fmt in CONFIG_FORMATS:
+        runs = [(fmt, "fp32") for fmt in CONFIG_FORMATS]
+        if shortcut:   # the shortcut rollback gate, method formats
+            runs += [(fmt, "shortcut") for fmt in FORMATS]
+        for fmt, gate in runs:
             cnt = torch.zeros(1, dtype=torch.int64, device=dev) if count else None
 
             def run():
                 if cnt is not None:
                     cnt.zero_()
-                fsa.attention_run(ws, o, fmt, THRESHOLD, rollback_count=cnt)
+                fsa.attention_run(ws, o, fmt, THRESHOLD, rollback_count=cnt, gate=gate)
             tq, ta = timed(lambda: fsa.attention_prepare(*qkv, ws, fmt), run)
-            r[fmt] = {"attention_ms": 1e3 * ta, "quantize_ms": 1e3 * tq,
+            key = fmt if gate == "fp32" else f"{fmt}_shortcut_gate"
+            r[key] = {"attention_ms": 1e3 * ta, "quantize_ms": 1e3 * tq,
                       "attention_tflops": F / ta / 1e12}
             if cnt is not None and fmt != "mxfp4_efq":
-                r[fmt]["rollback_count"] = int(cnt.item())
+                r[key]["rollback_count"] = int(cnt.item())
         if with_bf16:
             _, tb = timed(lambda: None, lambda: fsa.bf16_attention_fwd(*qkv, out=o))
             r["bf16"] = {"attention_ms": 1e3 * tb, "attention_tflops": F / tb / 1e12}
@@ -367,7 +371,7 @@ def run_configs(fsa, dev, stream, seed):
     mask[:, :, :16384] = False
     k[mask] = k[mask] * 8
     out["rollback-stress B=1 H=8 S=32768 D=128 (1 % of keys after 16384 x 8)"] = one(
-        "rollback-stress", 1, 8, 32768, 128, (q, k, v), True, count=True)
+        "rollback-stress", 1, 8, 32768, 128, (q, k, v), True, count=True, shortcut=True)
     del q, k, v, mask
     sweep = {}
     for S in SWEEP_S:
@@ -382,8 +386,9 @@ def add_config_fracs(configs, pk):
     """Each format's attention rate as a fraction of its roofline."""
     def walk(d):
         for key, val in d.items():
-            if key in CONFIG_FORMATS and isinstance(val, dict):
-                fmt = "mxfp4" if key == "mxfp4_efq" else key
+            base = key.replace("_shortcut_gate", "")
+            if base in CONFIG_FORMATS and isinstance(val, dict):
+                fmt = "mxfp4" if base == "mxfp4_efq" else base
                 val["frac_of_format_roofline"] = val["attention_tflops"] / format_roofline(pk, fmt)
                 val["frac_of_mx8_peak"] = val["attention_tflops"] / pk["mx8_sustained"]
             elif isinstance(val, dict):
@@ -497,6 +502,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-efq", action="store_true", help="skip the EFQ-Softmax format")
+    ap.add_argument("--no-shortcut", action="store_true", help="skip the shortcut-gate timing")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads (h16-s8192, rollback stress, the S sweep)")
     ap.add_argument("--no-mma-probe", action="store_true",
@@ -643,6 +649,28 @@ def main():
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error in the EFQ format")
 
+    # the shortcut rollback gate ("Fused-Softmax shifts ...", paragraph 12)
+    # against the FP32 gate on the same workload: the attention kernel alone
+    shortcut = None
+    if not args.no_shortcut and not cross:
+        shortcut = {}
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for fmt in FORMATS:
+            fsa.attention_prepare(tq, tk, tv, ws, fmt)
+            ts = []
+            for s_i in range(1 + max(1, args.steps // 2)):
+                ev[0].record(stream)
+                fsa.attention_run(ws, o, fmt, THRESHOLD, gate="shortcut")
+                ev[1].record(stream)
+                torch.cuda.synchronize(dev)
+                if s_i:
+                    ts.append(ev[0].elapsed_time(ev[1]) / 1e3)
+            ka = statistics.mean(ts)
+            shortcut[fmt] = {"attention_kernel_ms": 1e3 * ka, "attention_tflops": F / ka / 1e12,
+                             "vs_fp32_gate": per_format[fmt]["attention_kernel_ms"] / (1e3 * ka)}
+        if fsa.get_device_error() != 0:
+            raise RuntimeError("device error with the shortcut gate")
+
     # in-house BF16 flash-attention baseline, same inputs
     bf16 = None
     if not args.no_bf16 and not cross:  # the BF16 kernel is self-attention only
@@ -756,6 +784,7 @@ def main():
         "per_format": per_format,
         "bf16_baseline": bf16,
         "efq_format": efq,
+        "shortcut_gate": shortcut,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,

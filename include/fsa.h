@@ -112,6 +112,16 @@ typedef struct {
      * `stream` -- consecutive calls then overlap their copies.  0: the
      * copies wait for that work. */
     int host_inputs_ready;
+    /* Rollback gate ("Fused-Softmax shifts ...", paragraph 12): 0, the
+     * method's gate on the FP32 scores (a tile whose row maximum passes the
+     * reference by more than `threshold` rolls back); 1, the shortcut the
+     * pages' fastest four-bit kernel takes, gating on converted values: a tile
+     * rolls back when its largest P block scale under the current reference
+     * exceeds the scale of threshold's own weight code.  The shortcut is the
+     * FP32 gate at a threshold raised to the end of that scale's binade, so
+     * it misses the firings whose excess lies between the two.  Ignored by
+     * FSA_MXFP4_EFQ; other values: FSA_ERR_INVALID_ARGUMENT. */
+    int gate_mode;
 } fsa_options;
 
 /*

@@ -51,7 +51,10 @@ class Options(ctypes.Structure):
         ("efq_tau", ctypes.c_float),
         ("efq_h", ctypes.c_float),
         ("host_inputs_ready", ctypes.c_int),
+        ("gate_mode", ctypes.c_int),
     ]
+
+GATE_MODES = {"fp32": 0, "shortcut": 1}
 
 
 _lock = threading.Lock()
@@ -159,7 +162,7 @@ def workspace_size(B: int, H: int, S: int, D: int, fmt: str = "mxfp8") -> int:
 
 def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                   sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                  workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, debug_flags: int = 0, stream=None):
+                  workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, debug_flags: int = 0, gate: str = "fp32", stream=None):
     """Fused-Softmax MX attention forward (fsa_attention_fwd_ex).
 
     q, k, v: contiguous CUDA bf16 [B, H, S, D].  rollback_bits: optional uint8
@@ -177,6 +180,7 @@ def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=No
         opt.workspace = workspace.data_ptr()
         opt.workspace_bytes = workspace.numel() * workspace.element_size()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.wait_timeout_ms = wait_timeout_ms
     opt.debug_flags = debug_flags
     _check(load().fsa_attention_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
@@ -187,7 +191,7 @@ def attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=No
 
 def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                         sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                        workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+                        workspace=None, wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, gate: str = "fp32", stream=None):
     """fsa_cross_attention_fwd: q contiguous CUDA bf16 [B, H, Sq, D], k and v
     [B, H, Sk, D]; returns o [B, H, Sq, D].  rollback_bits: optional uint8
     CUDA tensor [B*H*Sq, ceil(Sk/128)]."""
@@ -206,6 +210,7 @@ def cross_attention_fwd(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, 
         opt.workspace = workspace.data_ptr()
         opt.workspace_bytes = workspace.numel() * workspace.element_size()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_cross_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
                                           FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -222,7 +227,7 @@ def _host_bhsd(t, name):
 def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                              sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
                              efq_tau: float = 0.0, efq_h: float = 0.0, host_inputs_ready: bool = False,
-                             stream=None):
+                             gate: str = "fp32", stream=None):
     """fsa_cross_attention_fwd_host: q, k, v contiguous HOST bf16 tensors
     ([B, H, Sq, D] and [B, H, Sk, D]; pinned memory lets the copies overlap
     the computation); returns the host output o [B, H, Sq, D] (or fills
@@ -245,6 +250,7 @@ def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.host_inputs_ready = int(bool(host_inputs_ready))
     _check(load().fsa_cross_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Sq, Sk, D,
                                                FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -255,7 +261,7 @@ def cross_attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0
 def attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, out=None,
                        sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
                        efq_tau: float = 0.0, efq_h: float = 0.0, host_inputs_ready: bool = False,
-                       stream=None):
+                       gate: str = "fp32", stream=None):
     """fsa_attention_fwd_host: self-attention on contiguous HOST bf16 tensors
     [B, H, S, D]; see cross_attention_fwd_host."""
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -272,6 +278,7 @@ def attention_fwd_host(q, k, v, fmt: str = "mxfp8", threshold: float = 8.0, *, o
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.host_inputs_ready = int(bool(host_inputs_ready))
     _check(load().fsa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, S, D,
                                          FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -301,7 +308,7 @@ def cross_attention_prepare(q, k, v, workspace, fmt: str = "mxfp8", stream=None)
 
 def cross_attention_run(workspace, out, Sk: int, fmt: str = "mxfp8", threshold: float = 8.0, *,
                         sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                        wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+                        wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, gate: str = "fp32", stream=None):
     """Second half of cross_attention_fwd: `out` [B, H, Sq, D] fixes B, H, Sq and D;
     Sk is the key length given to cross_attention_prepare."""
     _bhsd(out, "out")
@@ -311,6 +318,7 @@ def cross_attention_run(workspace, out, Sk: int, fmt: str = "mxfp8", threshold: 
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_cross_attention_run(_ptr(workspace), workspace.numel(), _ptr(out), B, H, Sq,
                                           Sk, D, FORMATS[fmt], float(threshold), ctypes.byref(opt),
@@ -335,7 +343,7 @@ def attention_prepare(q, k, v, workspace, fmt: str = "mxfp8", stream=None):
 
 def attention_run(workspace, out, fmt: str = "mxfp8", threshold: float = 8.0, *,
                   sm_scale: float = 0.0, rollback_bits=None, rollback_count=None,
-                  wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, stream=None):
+                  wait_timeout_ms: int = 0, efq_tau: float = 0.0, efq_h: float = 0.0, gate: str = "fp32", stream=None):
     """Second half of attention_fwd: the fused kernel on a prepared workspace;
     `out` is the bf16 [B, H, S, D] output and fixes the shape."""
     _bhsd(out, "out")
@@ -345,6 +353,7 @@ def attention_run(workspace, out, fmt: str = "mxfp8", threshold: float = 8.0, *,
     opt.rollback_bits = None if rollback_bits is None else rollback_bits.data_ptr()
     opt.rollback_count = None if rollback_count is None else rollback_count.data_ptr()
     opt.efq_tau, opt.efq_h = efq_tau, efq_h
+    opt.gate_mode = GATE_MODES[gate]
     opt.wait_timeout_ms = wait_timeout_ms
     _check(load().fsa_attention_run(_ptr(workspace), workspace.numel(), _ptr(out), B, H, S, D,
                                     FORMATS[fmt], float(threshold), ctypes.byref(opt),

@@ -41,6 +41,9 @@
 // E4M3's grid shifted by 2^6 from its subnormal step up to its maximum).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include "fsa_internal.h"
 #include "sm100_ptx.cuh"
 
@@ -125,6 +128,7 @@ struct Params {
     float alpha;     // 128 * log2(e) * sm_scale
     float theta;     // gate threshold, natural-log score units
     float theta_raw; // theta / sm_scale: the same threshold on accumulator values
+    int sb_theta;    // shortcut gate: the P block scale byte of theta's own weight code
     uint64_t timeout_ns;
     int debug_flags;
     // 2^8 and 2^16, held in registers: byte and half-word packing as an
@@ -287,6 +291,23 @@ __device__ __forceinline__ int block_scale_byte(float bmax, float alpha, float b
     const float y = fmaxf(__fmaf_rn(bmax, alpha, beta), -1.0f);
     const int c = static_cast<int>(__float_as_uint(__fadd_rn(y, kMagic))) - kMagicBits;
     return max((c + 127 - static_cast<int>(T::kMthr) - 128 * T::kEmax) >> 7, 0) + T::kOff;
+}
+
+// The rollback gate of a tile whose row maximum is tmax (accumulator units)
+// against the reference m.  The method's gate compares the FP32 scores: tmax
+// - m > theta.  The shortcut ("Fused-Softmax shifts ...", paragraph 12: the
+// fastest four-bit kernel gates on converted values and can miss a trigger)
+// fires when the tile's largest P block scale under the current reference --
+// the scale byte of the block holding tmax -- exceeds the scale byte of
+// theta's own weight code, i.e. the FP32 gate at a threshold raised to the
+// end of theta's scale binade.
+template <bool kShortcut, bool kE4M3>
+__device__ __forceinline__ bool gate_fires(float tmax, float m, float alpha, float theta_raw,
+                                           int sb_theta) {
+    if constexpr (kShortcut)
+        return block_scale_byte<kE4M3>(tmax, alpha, 16249.0f - alpha * m) > sb_theta;
+    else
+        return tmax - m > theta_raw;
 }
 
 // E4M3 P: a block converts to E4M3 normals when its smallest code is a
@@ -555,7 +576,7 @@ __device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float r
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
-template <int kP>
+template <int kP, bool kShortcut = false>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int g, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
                                              bool row_valid, int64_t grow, bool tail, bool bounded,
@@ -689,13 +710,14 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
                 prev = sm.tmax_x[ms][r];
             }
-            if (t == 1 || prev - rs.m_acc > p.theta_raw) rs.m_acc = prev;
+            if (t == 1 || gate_fires<kShortcut, kE4M3>(prev, rs.m_acc, p.alpha, p.theta_raw, p.sb_theta))
+                rs.m_acc = prev;
         }
         bool fire = false;
         float rescale = 1.0f;
         if (t == 0) {
             rs.m_acc = tmax;
-        } else if (tmax - rs.m_acc > p.theta_raw) {
+        } else if (gate_fires<kShortcut, kE4M3>(tmax, rs.m_acc, p.alpha, p.theta_raw, p.sb_theta)) {
             fire = true;
             rescale = expf((rs.m_acc - tmax) * p.sm_scale);
             rs.m_acc = tmax;
@@ -730,7 +752,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <int kP>
+template <int kP, bool kShortcut = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -968,8 +990,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool bounded = false;
         if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
-            ok = softmax_tile<kP>(sm, p, t, t, it, wg, r, lane_addr, s_col, row_valid, grow, t == t_tail,
-                                  bounded, rs);
+            ok = softmax_tile<kP, kShortcut>(sm, p, t, t, it, wg, r, lane_addr, s_col, row_valid, grow,
+                                             t == t_tail, bounded, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
             ok = wait_warp(&sm.o_full, 0, p, sm);
@@ -1387,6 +1409,15 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     p.alpha = static_cast<float>(128.0 * 1.4426950408889634 * static_cast<double>(a.sm_scale));
     p.theta = a.threshold;
     p.theta_raw = a.threshold / a.sm_scale;
+    {
+        // theta's own weight code and its P block scale byte (as
+        // block_scale_byte computes it: E4M3 P for MXFP8, six-bit P with its
+        // offset of 6 otherwise)
+        const double y = 128.0 * (static_cast<double>(a.threshold) * 1.4426950408889634 + 127.0) - 7.0;
+        const int c = static_cast<int>(std::nearbyint(y < 0x7F7F ? y : 0x7F7F));
+        p.sb_theta = a.fmt == 0 ? std::max((c + 127 - 0x60 - 128 * 8) >> 7, 0)
+                                : std::max((c + 127 - 0x70 - 128 * 2) >> 7, 0) + 6;
+    }
     p.timeout_ns = a.timeout_ns;
     p.debug_flags = a.debug_flags;
     p.mul8 = 1u << 8;
@@ -1408,7 +1439,9 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     // short key sequences: the per-CTA set-up and pipeline fill would
     // dominate a CTA that runs only a few KV tiles, so one persistent CTA per
     // SM walks the work items instead
-    const bool persistent = p.n_t <= kPersistentMaxTiles && n_items > n_sm;
+    // the shortcut gate exists as a variant of the one-CTA-per-item kernel
+    const bool shortcut = a.gate_mode == 1 && a.fmt != 3;
+    const bool persistent = !shortcut && p.n_t <= kPersistentMaxTiles && n_items > n_sm;
     // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4, E2M1 codes of
     // the EFQ producer for MXFP4-EFQ
     using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
@@ -1417,6 +1450,8 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
         kernel = a.fmt == 0 ? fsa_attn_fwd_persistent_kernel<kPE4M3>
                             : (a.fmt == 3 ? fsa_attn_fwd_persistent_kernel<kPEfq>
                                           : fsa_attn_fwd_persistent_kernel<kPE2M3>);
+    else if (shortcut)
+        kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<kPE4M3, true> : fsa_attn_fwd_kernel<kPE2M3, true>;
     else
         kernel = a.fmt == 0 ? fsa_attn_fwd_kernel<kPE4M3>
                             : (a.fmt == 3 ? fsa_attn_fwd_kernel<kPEfq> : fsa_attn_fwd_kernel<kPE2M3>);

@@ -171,6 +171,7 @@ fsa_status check_run_args(int fmt, float threshold, const fsa_options& op) {
     if (!std::isfinite(op.sm_scale)) return FSA_ERR_INVALID_ARGUMENT;
     if (fmt == FSA_MXFP4_EFQ && (!std::isfinite(op.efq_tau) || !std::isfinite(op.efq_h)))
         return FSA_ERR_INVALID_ARGUMENT;
+    if (op.gate_mode != 0 && op.gate_mode != 1) return FSA_ERR_INVALID_ARGUMENT;
     return FSA_OK;
 }
 
@@ -237,6 +238,7 @@ fsa_status run_impl(void* ws_base, void* o, int64_t BH, int Sq, int Sk, int D, i
     a.timeout_ns = static_cast<uint64_t>(op.wait_timeout_ms > 0 ? op.wait_timeout_ms : 2000) *
                    1000000ull;
     a.debug_flags = op.debug_flags;
+    a.gate_mode = op.gate_mode;
     a.err_word = err;
     // the kernel writes only the bytes of firings
     if (op.rollback_bits &&

@@ -65,6 +65,7 @@ struct AttnLaunch {
     unsigned long long* rollback_count;
     uint64_t timeout_ns;
     int debug_flags;
+    int gate_mode;  // 0: FP32 gate, 1: shortcut on the P block scale
     unsigned int* err_word;
 };
 cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st);
