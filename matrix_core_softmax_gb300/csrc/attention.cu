@@ -586,49 +586,106 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
     tc_fence_after();
     uint32_t s0[32], s1[32], s2[32], s3[32];
-    tmem_ld32(s_col, s0);
-    tmem_ld32(s_col + 32, s1);
-    // while the scores travel: non-blocking looks at the other warpgroup's
-    // maximum of tile t - 1 and at this tile's P buffer (PV of the CTA's
-    // tile g - 2 retired); both are normally complete by now.  Buffers,
-    // slots and barrier phases follow the CTA's running tile count g (g = t
-    // when a CTA processes one work item); the method's tile logic follows
-    // t, the tile's index within its work item.
+    // Buffers, slots and barrier phases follow the CTA's running tile count
+    // g (g = t when a CTA processes one work item); the method's tile logic
+    // follows t, the tile's index within its work item.
     const int ms = (g - 1) & 7;
     const uint32_t m_par = ((g - 1) >> 3) & 1;
     const uint32_t pf_par = ((g >> 1) - 1) & 1;
-    const bool have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
-    float prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
-    const bool have_p = g < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
-    tmem_ld_wait();
-    tmem_reg_dep(s0);
-    tmem_reg_dep(s1);
-    // the second half travels while the first is reduced
-    tmem_ld32(s_col + 64, s2);
-    tmem_ld32(s_col + 96, s3);
-    float h_max0, h_min0 = 0.0f, h_max1, h_min1 = 0.0f;
-    // the EFQ producer needs no minima; six-bit P takes them in a second pass
-    // only where its norm bound does not hold
-    if constexpr (kP != kPE4M3) {
-        h_max0 = max32(s0);
-        h_max1 = max32(s1);
-    } else {
-        maxmin32(s0, h_max0, h_min0);
-        maxmin32(s1, h_max1, h_min1);
+    bool have_prev, have_p;
+    float prev;
+    // The block maxima (and minima where the conversion needs them) of the
+    // row's four 32-key blocks.  The EFQ producer needs no minima; six-bit P
+    // takes them only where its norm bound does not hold (and on the tail).
+    float bmax[4], bmin[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const bool need_min = kP == kPE4M3 || (kP == kPE2M3 && (!bounded || tail));
+    bool extrema_done = false;
+#if defined(FSA_HAVE_TMEM_REDUCE) && !defined(FSA_NO_TMEM_REDUCE)
+    if (!tail) {
+        // sm_103a: the reducing TMEM load returns each block's maximum with
+        // its scores, so the maxima take no instruction on the CUDA cores.
+        // (A second reducing load per block for the minima was measured
+        // slower than the three-input minimum tree below.)
+        tmem_ld32_red<true>(s_col, s0, bmax[0]);
+        tmem_ld32_red<true>(s_col + 32, s1, bmax[1]);
+        tmem_ld32_red<true>(s_col + 64, s2, bmax[2]);
+        tmem_ld32_red<true>(s_col + 96, s3, bmax[3]);
+        // while the scores travel: non-blocking looks at the other
+        // warpgroup's maximum of tile t - 1 and at this tile's P buffer (PV
+        // of the CTA's tile g - 2 retired); both are normally complete by now
+        have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
+        prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
+        have_p = g < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
+        tmem_ld_wait();
+        tmem_reg_dep(s0);
+        tmem_reg_dep(s1);
+        tmem_reg_dep(s2);
+        tmem_reg_dep(s3);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tmem_reg_dep1(bmax[b]);
+        if (need_min) {
+            bmin[0] = min32(s0);
+            bmin[1] = min32(s1);
+            bmin[2] = min32(s2);
+            bmin[3] = min32(s3);
+        }
+        extrema_done = true;
+    } else
+#endif
+    {
+        tmem_ld32(s_col, s0);
+        tmem_ld32(s_col + 32, s1);
+        // while the scores travel: the looks at the other warpgroup's
+        // maximum and at this tile's P buffer, as above
+        have_prev = t == 0 || mbar_test(&sm.m_ready[ms], m_par);
+        prev = (t > 0 && have_prev) ? sm.tmax_x[ms][r] : 0.0f;
+        have_p = g < kPBuf || mbar_test(&sm.p_free[pb], pf_par);
+        tmem_ld_wait();
+        tmem_reg_dep(s0);
+        tmem_reg_dep(s1);
+        // the second half travels while the first is reduced (the tail tile
+        // reduces after masking, below)
+        tmem_ld32(s_col + 64, s2);
+        tmem_ld32(s_col + 96, s3);
+        if (!tail) {
+            if (need_min) {
+                maxmin32(s0, bmax[0], bmin[0]);
+                maxmin32(s1, bmax[1], bmin[1]);
+            } else {
+                bmax[0] = max32(s0);
+                bmax[1] = max32(s1);
+            }
+        }
+        tmem_ld_wait();
+        tmem_reg_dep(s2);
+        tmem_reg_dep(s3);
     }
-    tmem_ld_wait();
-    tmem_reg_dep(s2);
-    tmem_reg_dep(s3);
     // the whole tile is in registers: the next score product may reuse S
     tc_fence_before();
     warp_arrive(&sm.s_free[wg]);
-    if (tail) {
-        // keys >= S of a partial last tile are masked before the gate and the conversion
-        const int n_valid = p.Sk - t * kTile;
-        mask32(s0, n_valid);
-        mask32(s1, n_valid - 32);
-        mask32(s2, n_valid - 64);
-        mask32(s3, n_valid - 96);
+    if (!extrema_done) {
+        if (tail) {
+            // keys >= S of a partial last tile are masked before the gate and the conversion
+            const int n_valid = p.Sk - t * kTile;
+            mask32(s0, n_valid);
+            mask32(s1, n_valid - 32);
+            mask32(s2, n_valid - 64);
+            mask32(s3, n_valid - 96);
+            if (need_min) {
+                maxmin32(s0, bmax[0], bmin[0]);
+                maxmin32(s1, bmax[1], bmin[1]);
+            } else {
+                bmax[0] = max32(s0);
+                bmax[1] = max32(s1);
+            }
+        }
+        if (need_min) {
+            maxmin32(s2, bmax[2], bmin[2]);
+            maxmin32(s3, bmax[3], bmin[3]);
+        } else {
+            bmax[2] = max32(s2);
+            bmax[3] = max32(s3);
+        }
     }
     uint32_t w0[8], w1[8], w2[8], w3[8];
     uint32_t sfw;
@@ -637,10 +694,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // Online Attention"): the running row maximum, replayed over the
         // other warpgroup's maximum of tile t - 1, and O, l rescaled exactly
         // when it grows
-        // the first half's maxima were taken while the second half loaded
-        // (again after the tail mask)
-        const float bm0 = tail ? max32(s0) : h_max0, bm1 = tail ? max32(s1) : h_max1;
-        const float bm2 = max32(s2), bm3 = max32(s3);
+        const float bm0 = bmax[0], bm1 = bmax[1], bm2 = bmax[2], bm3 = bmax[3];
         const float tmax = fmaxf(fmaxf(bm0, bm1), fmaxf(bm2, bm3));
         sm.tmax_x[g & 7][r] = tmax;
         warp_arrive(&sm.m_ready[g & 7]);
@@ -670,31 +724,9 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         }
     } else {
         constexpr bool kE4M3 = kP == kPE4M3;
-        float bmax[4] = {h_max0, h_max1, 0.0f, 0.0f}, bmin[4] = {h_min0, h_min1, 0.0f, 0.0f};
         // a bounded six-bit warp needs only the block maxima, except on the
         // tail tile, whose masked keys take the general conversion
         const bool no_min = !kE4M3 && bounded && !tail;
-        if constexpr (kE4M3) {
-            if (tail) {  // the masked keys change the first half's extrema too
-                maxmin32(s0, bmax[0], bmin[0]);
-                maxmin32(s1, bmax[1], bmin[1]);
-            }
-            maxmin32(s2, bmax[2], bmin[2]);
-            maxmin32(s3, bmax[3], bmin[3]);
-        } else {
-            if (tail) {
-                bmax[0] = max32(s0);
-                bmax[1] = max32(s1);
-            }
-            bmax[2] = max32(s2);
-            bmax[3] = max32(s3);
-            if (!no_min) {  // rare: the exact test of the scaled conversion needs the minima
-                bmin[0] = min32(s0);
-                bmin[1] = min32(s1);
-                bmin[2] = min32(s2);
-                bmin[3] = min32(s3);
-            }
-        }
         const float tmax = fmaxf(fmaxf(bmax[0], bmax[1]), fmaxf(bmax[2], bmax[3]));
         // publish this tile's row maximum for the other warpgroup in slot g % 8;
         // the reader consumes it during its tile g + 1, long before this

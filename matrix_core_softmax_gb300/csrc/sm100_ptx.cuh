@@ -249,6 +249,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : FSA_R8(0), FSA_R8(8)
         : "r"(taddr));
 }
+// sm_103a's reducing TMEM load: as tmem_ld32, and `red` receives the largest
+// (kMax) or smallest of the 32 values this thread loads, i.e. the maximum or
+// minimum over 32 columns of its TMEM lane.  `red` is valid after the same
+// tcgen05.wait::ld as the loaded registers.
+#if defined(__CUDA_ARCH_FEAT_SM103_ALL) || !defined(__CUDA_ARCH__)
+template <bool kMax>
+__device__ __forceinline__ void tmem_ld32_red(uint32_t taddr, uint32_t (&r)[32], float& red) {
+    if constexpr (kMax)
+        asm volatile(
+            "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+            : FSA_R8(0), FSA_R8(8), FSA_R8(16), FSA_R8(24), "=f"(red)
+            : "r"(taddr));
+    else
+        asm volatile(
+            "tcgen05.ld.red.sync.aligned.32x32b.x32.min.f32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+            : FSA_R8(0), FSA_R8(8), FSA_R8(16), FSA_R8(24), "=f"(red)
+            : "r"(taddr));
+}
+#define FSA_HAVE_TMEM_REDUCE 1
+#endif
 #undef FSA_R8
 __device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t& r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
@@ -302,6 +326,8 @@ __device__ __forceinline__ void tmem_reg_dep(uint32_t (&r)[32]) {
     asm volatile("" : FSA_D8(0), FSA_D8(8), FSA_D8(16), FSA_D8(24) : : "memory");
 }
 #undef FSA_D8
+// As tmem_reg_dep for one FP32 value (a reducing load's result).
+__device__ __forceinline__ void tmem_reg_dep1(float& x) { asm volatile("" : "+f"(x) : : "memory"); }
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
