@@ -62,7 +62,7 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegs <= kThreads * kLaunchRe
               "register split exceeds the launch allocation");
 // Work items of at most this many KV tiles go to the persistent kernel
 // (measured on GB300 with 75600 query rows x 40 heads: faster up to 2048
-// keys, even at 4096, slower at 8192).
+// keys, even at 4096, slower at 8192), whatever the number of items.
 constexpr int kPersistentMaxTiles = 16;
 // The persistent kernel's helper warps keep the rings' state across work
 // items and give back only to 40: 2 * 128 * 232 + 128 * 40 = 64512.
@@ -425,7 +425,7 @@ __device__ __forceinline__ uint32_t efq_block(const uint32_t (&v)[32], float bma
 // block scales from the block maxima, then the E4M3 patterns of the row in
 // w0..w3 (keys 32 b .. 32 b + 31 in w_b).  Returns the four E8M0 scale bytes
 // packed into a word.
-template <bool kE4M3>
+template <bool kE4M3, bool kSpec>
 __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
                                                  const uint32_t (&s2)[32], const uint32_t (&s3)[32],
                                                  const float (&bmax)[4], const float (&bmin)[4],
@@ -436,13 +436,34 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
     const int sb1 = block_scale_byte<kE4M3>(bmax[1], alpha, beta);
     const int sb2 = block_scale_byte<kE4M3>(bmax[2], alpha, beta);
     const int sb3 = block_scale_byte<kE4M3>(bmax[3], alpha, beta);
+    if constexpr (kE4M3 && kSpec) {
+        // E4M3 P: the linear conversion first (the common case), the test
+        // that every element of the warp's rows is an E4M3 normal after it,
+        // so the minimum tree overlaps the conversion; redone by the general
+        // conversion when the test fails (rare).  (The persistent kernel
+        // takes the test first: this order costs it registers.)
+        convert32_linear(s0, alpha, beta, linear_kx(sb0), linear_kx2(sb0), mul8, mul16, w0);
+        convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
+        convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
+        convert32_linear(s3, alpha, beta, linear_kx(sb3), linear_kx2(sb3), mul8, mul16, w3);
+        if ((!__all_sync(0xFFFFFFFFu,
+                                     block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                                     max(max(sb0, sb1), max(sb2, sb3)), alpha, beta)))) {
+            convert32<true>(s0, alpha, beta, general_inv(sb0), mul16, w0);
+            convert32<true>(s1, alpha, beta, general_inv(sb1), mul16, w1);
+            convert32<true>(s2, alpha, beta, general_inv(sb2), mul16, w2);
+            convert32<true>(s3, alpha, beta, general_inv(sb3), mul16, w3);
+        }
+        return (static_cast<uint32_t>(sb0) + static_cast<uint32_t>(sb1) * mul8) +
+               (static_cast<uint32_t>(sb2) + static_cast<uint32_t>(sb3) * mul8) * mul16;
+    }
     // one decision for the whole tile: every row of the warp converts
     // linearly (the common case for MXFP8), else block by block.  Checked
     // once per row against the largest block threshold (sb grows with the
     // block maximum), which implies every block's own condition.
-    if (kE4M3 && __all_sync(0xFFFFFFFFu,
+    if (kE4M3 && (__all_sync(0xFFFFFFFFu,
                             block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
-                                            max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
+                                            max(max(sb0, sb1), max(sb2, sb3)), alpha, beta)))) {
         convert32_linear(s0, alpha, beta, linear_kx(sb0), linear_kx2(sb0), mul8, mul16, w0);
         convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
@@ -569,6 +590,51 @@ __device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float r
     tmem_st_wait();
 }
 
+// Epilogue of one row of the persistent kernel: warpgroup wg writes columns
+// [wg * D/2, (wg+1) * D/2) of o = O / l as bf16, one 32-column chunk of O at
+// a time.  `o_free`, when given, is released as soon as the last chunk and l
+// are read from TMEM (the next work item's first PV product may then
+// overwrite O while the last division and stores run).  The division is a
+// multiplication by the IEEE reciprocal of l (within 1.5 units in the last
+// FP32 place of O / l, before the bf16 rounding): on items of a few KV tiles
+// an IEEE division per element cost a third of the item's instructions
+// (measured 785 -> 1086 TFLOP/s with four tiles per item).  The one-CTA
+// kernel divides (once per CTA of many tiles it costs nothing, and its main
+// loop measured faster so compiled); which kernel a call takes depends only
+// on the key length, so calls with the same keys compute the same bytes.
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&rr)[32], float l, uint4* dst) {
+    const float inv = __frcp_rn(l);
+    uint32_t packed[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(rr[2 * j]) * inv,
+                                                  __uint_as_float(rr[2 * j + 1]) * inv);
+        packed[j] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+}
+
+__device__ __forceinline__ void epilogue_row(uint32_t lane_addr, int D, int wg, bool row_valid,
+                                             __nv_bfloat16* o_row, uint64_t* o_free) {
+    tc_fence_after();
+    const int c0 = wg * (D / 64), c1 = (wg + 1) * (D / 64);  // this warpgroup's 32-column chunks
+    uint32_t rr[32], lv;
+    tmem_ld1(lane_addr + kColO + D, lv);
+    for (int c = c0; c < c1; ++c) {
+        tmem_ld32(lane_addr + kColO + 32 * c, rr);
+        tmem_ld_wait();
+        tmem_reg_dep(rr);
+        if (c + 1 == c1 && o_free) {
+            tc_fence_before();
+            warp_arrive(o_free);
+        }
+        if (row_valid)
+            epilogue_chunk(rr, __uint_as_float(lv), reinterpret_cast<uint4*>(o_row + 32 * c));
+    }
+}
+
 // One KV tile t (the it-th of warpgroup wg) for query row r: read the 128
 // scores once (one TMEM wait), release the S buffer, block max/min, the
 // reference hand-off and the gate (with the O / l rescale on a rollback),
@@ -576,7 +642,7 @@ __device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float r
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
-template <int kP, bool kShortcut = false>
+template <int kP, bool kShortcut = false, bool kSpec = false>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int g, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
                                              bool row_valid, int64_t grow, bool tail, bool bounded,
@@ -664,7 +730,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tc_fence_before();
     warp_arrive(&sm.s_free[wg]);
     if (!extrema_done) {
-        if (tail) {
+        if ((tail)) {
             // keys >= S of a partial last tile are masked before the gate and the conversion
             const int n_valid = p.Sk - t * kTile;
             mask32(s0, n_valid);
@@ -699,7 +765,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         sm.tmax_x[g & 7][r] = tmax;
         warp_arrive(&sm.m_ready[g & 7]);
         if (t > 0) {
-            if (!have_prev) {
+            if ((!have_prev)) {
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
                 prev = sm.tmax_x[ms][r];
             }
@@ -717,7 +783,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // the running maximum grows on a large share of tiles: O and l are
         // rescaled after the conversion, so that the wait for the previous
         // PV product overlaps it (P buffer first, as below)
-        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if ((!have_p)) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
         if (any_grew) {
             ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o_all(lane_addr, D, rescale);
@@ -738,7 +804,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // frozen reference: replay the gate over the previous tile's maximum,
         // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
         if (t > 0) {
-            if (!have_prev) {
+            if ((!have_prev)) {
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
                 prev = sm.tmax_x[ms][r];
             }
@@ -758,8 +824,8 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // products retire in order, so afterwards the barrier of tile g - 1's
         // buffer is past PV_{g-3} and can only be in the phase of PV_{g-1}
         // itself (PV_{g+1} needs this tile's P).
-        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
-        if (__any_sync(0xFFFFFFFFu, fire)) {
+        if ((!have_p)) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if ((__any_sync(0xFFFFFFFFu, fire))) {
             // the bitmap was zeroed before the launch: only firings are written
             if (fire && row_valid) {
                 if (p.rollback_bits) p.rollback_bits[grow * p.n_t + t] = 1;
@@ -770,7 +836,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o(lane_addr, D, rescale);
         }
-        sfw = convert_tile<kE4M3>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc,
+        sfw = convert_tile<kE4M3, kSpec>(s0, s1, s2, s3, bmax, bmin, p.alpha, 16249.0f - p.alpha * rs.m_acc,
                                   p.mul8, p.mul16, no_min, w0, w1, w2, w3);
     }
     // the P row into TMEM (the A operand of the PV product) and its four
@@ -1022,8 +1088,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool bounded = false;
         if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
         for (int t = wg, it = 0; ok && t < p.n_t; t += 2, ++it)
-            ok = softmax_tile<kP, kShortcut>(sm, p, t, t, it, wg, r, lane_addr, s_col, row_valid, grow,
-                                             t == t_tail, bounded, rs);
+            ok = softmax_tile<kP, kShortcut, true>(sm, p, t, t, it, wg, r, lane_addr, s_col, row_valid,
+                                                   grow, t == t_tail, bounded, rs);
         if (!ok) raise_abort(sm, p);
         if (ok) {
             ok = wait_warp(&sm.o_full, 0, p, sm);
@@ -1351,52 +1417,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int it = 0;  // tiles this warpgroup processed (phase of its S buffer)
         RowState rs{0.0f, 0u};  // the firing count runs over all items
+        // The epilogue of item j - 1 is owed while item j starts: the
+        // warpgroup whose first tile of item j is tile 0 converts that tile
+        // first (it needs no reference, gate or rescale, so it waits on
+        // nothing the owed epilogue holds back), while the last PV product of
+        // item j - 1 completes; the other warpgroup writes its half first,
+        // since its first tile (1) may roll back and wait for PV of tile 0,
+        // which waits for both halves of the epilogue (o_free).
+        bool owed = false;
+        bool owed_valid = false;
+        int64_t owed_grow = 0;
         for (int j = 0; ok; ++j) {
             const int item = blockIdx.x + j * gridDim.x;
-            if (item >= p.n_items) break;
+            const bool have = item < p.n_items;
             const int g0 = j * p.n_t;  // running count of the item's tile 0
-            const int bh = item / p.n_qt;
-            const int q0 = (item - bh * p.n_qt) * kTile;
-            const bool row_valid = (q0 + r) < p.Sq;
+            const int bh = have ? item / p.n_qt : 0;
+            const int q0 = have ? (item - bh * p.n_qt) * kTile : 0;
+            const bool row_valid = have && (q0 + r) < p.Sq;
             const int64_t grow = static_cast<int64_t>(bh) * p.Sq + q0 + r;
             // six-bit P: a warp whose rows satisfy the norm bound skips the block minima
             bool bounded = false;
-            if constexpr (kP == kPE2M3) bounded = warp_bounded(p, bh, row_valid, grow);
+            if constexpr (kP == kPE2M3) {
+                if (have) bounded = warp_bounded(p, bh, row_valid, grow);
+            }
             rs.m_acc = 0.0f;
-            for (int t = (wg - g0) & 1; ok && t < p.n_t; t += 2, ++it)
+            const int t0 = (wg - g0) & 1;  // this warpgroup's first tile of the item
+            // O and l of item j - 1 are released to item j's first PV product
+            // as soon as they are read
+            if (owed && !(have && t0 == 0)) {
+                if (ok) ok = wait_warp(&sm.o_full, (j - 1) & 1, p, sm);
+                if (!ok) break;
+                epilogue_row(lane_addr, D, wg, owed_valid, p.o + owed_grow * D, &sm.o_free);
+                owed = false;
+            }
+            if (!have) break;
+            for (int t = t0; ok && t < p.n_t; t += 2, ++it) {
                 ok = softmax_tile<kP>(sm, p, t, g0 + t, it, wg, r, lane_addr, s_col, row_valid, grow,
                                       t == t_tail, bounded, rs);
-            if (ok) ok = wait_warp(&sm.o_full, j & 1, p, sm);
-            if (!ok) break;
-            // epilogue: warpgroup wg writes columns [wg * D/2, (wg+1) * D/2)
-            tc_fence_after();
-            uint32_t lv;
-            tmem_ld1(lane_addr + kColO + D, lv);
-            tmem_ld_wait();
-            const float l = __uint_as_float(lv);
-            for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
-                uint32_t rr[32];
-                tmem_ld32(lane_addr + kColO + 32 * c, rr);
-                tmem_ld_wait();
-                tmem_reg_dep(rr);
-                if (row_valid) {
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * jj]), l),
-                                                                  __fdiv_rn(__uint_as_float(rr[2 * jj + 1]), l));
-                        packed[jj] = *reinterpret_cast<uint32_t*>(&h2);
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + 32 * c);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        dst[jj] = make_uint4(packed[4 * jj], packed[4 * jj + 1], packed[4 * jj + 2],
-                                             packed[4 * jj + 3]);
+                if (owed) {  // deferred past tile 0
+                    if (ok) ok = wait_warp(&sm.o_full, (j - 1) & 1, p, sm);
+                    if (ok) epilogue_row(lane_addr, D, wg, owed_valid, p.o + owed_grow * D, &sm.o_free);
+                    owed = false;
                 }
             }
-            // O and l are read: the next item's first PV product may overwrite them
-            tc_fence_before();
-            warp_arrive(&sm.o_free);
+            owed = true;
+            owed_valid = row_valid;
+            owed_grow = grow;
         }
         if (!ok) raise_abort(sm, p);
         if (ok && p.rollback_count) {
@@ -1469,11 +1535,14 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     // short key sequences: the per-CTA set-up and pipeline fill would
-    // dominate a CTA that runs only a few KV tiles, so one persistent CTA per
-    // SM walks the work items instead
+    // dominate a CTA that runs only a few KV tiles, so persistent CTAs (one
+    // per SM, at most one per work item) walk the work items instead.  The
+    // choice depends on the key length alone, not on the number of items,
+    // so every call with the same keys -- a whole tensor or the chunks of
+    // heads of the host-buffer entry points -- takes the same kernel
     // the shortcut gate exists as a variant of the one-CTA-per-item kernel
     const bool shortcut = a.gate_mode == 1 && a.fmt != 3;
-    const bool persistent = !shortcut && p.n_t <= kPersistentMaxTiles && n_items > n_sm;
+    const bool persistent = !shortcut && p.n_t <= kPersistentMaxTiles;
     // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4, E2M1 codes of
     // the EFQ producer for MXFP4-EFQ
     using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);
@@ -1496,7 +1565,8 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (persistent) {
-        kernel<<<static_cast<unsigned>(n_sm), kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
+        const int ctas = n_items < n_sm ? static_cast<int>(n_items) : n_sm;
+        kernel<<<static_cast<unsigned>(ctas), kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);
     } else {
         dim3 grid(static_cast<unsigned>(p.n_qt), static_cast<unsigned>(a.BH));
         kernel<<<grid, kThreads, smem, st>>>(*a.tm_q, *a.tm_k, *a.tm_v, p);

@@ -45,8 +45,11 @@ def _run(fsa, q, k, v, fmt, theta=8.0, want_bits=False):
     return o, rb, int(cnt.item())
 
 
+# up to 2048 keys (16 KV tiles) the persistent kernel runs; beyond, one CTA
+# per (query tile, head): 2049 and 2200 keys put a ragged tail of 1 and 24
+# keys on the one-CTA kernel
 SMALL = [(1, 2, 512, 64), (1, 1, 1, 64), (1, 2, 31, 128), (2, 1, 33, 64), (1, 1, 129, 128),
-         (1, 3, 300, 64), (1, 1, 1000, 128), (2, 2, 257, 128)]
+         (1, 3, 300, 64), (1, 1, 1000, 128), (2, 2, 257, 128), (1, 1, 2049, 128), (1, 2, 2200, 64)]
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp6", "mxfp4"])
@@ -111,7 +114,9 @@ def test_bf16_kernel_matches_exact_attention(fsa, shape):
 def test_bounded_wait_reports_timeout_and_context_survives(fsa):
     # the loader skips KV tile 1: every wait on it must give up, the kernel
     # must exit cleanly, and the next call on the same context must work
-    B, H, S, D = 1, 1, 512, 64
+    # (18 KV tiles: the one-CTA-per-item kernel; the persistent kernel's own
+    # case is in test_gpu_persistent.py)
+    B, H, S, D = 1, 1, 2304, 64
     q, k, v = fsa_inputs.qkv(B, H, S, D, seed=2)
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     fsa.attention_fwd(tq, tk, tv, fmt="mxfp8", wait_timeout_ms=200,

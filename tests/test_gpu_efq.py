@@ -23,7 +23,7 @@ def fsa():
     return m
 
 
-SMALL = [(1, 2, 512, 64), (1, 1, 1, 64), (1, 2, 31, 128), (2, 1, 33, 64), (1, 1, 129, 128),
+SMALL = [(1, 1, 2049, 128), (1, 2, 512, 64), (1, 1, 1, 64), (1, 2, 31, 128), (2, 1, 33, 64), (1, 1, 129, 128),
          (1, 3, 300, 64), (1, 1, 1000, 128), (2, 2, 257, 128)]
 
 
