@@ -412,27 +412,28 @@ __global__ void __launch_bounds__(256) quant_rows_attn_kernel(
     }
 }
 
-// V: blocks of 32 keys, written transposed.  One thread per pair of
-// columns and 32 keys: 32 four-byte loads (a warp reads 128 contiguous bytes
-// of a key row per load), the two columns split by byte permutes, two blocks
-// quantized, 32 contiguous code bytes written to each of the two transposed
-// lines.
+// V of the fused attention (blocks of 32 keys along the keys, output
+// transposed: codes [batch][cols][pitch] with the keys contiguous), one
+// 128-key tile of one head per CTA and a thread per column pair and 32-key
+// block: the tile's codes are assembled in shared memory ([column][key], rows
+// padded to 144 bytes against bank conflicts) and written out as whole
+// 128-byte lines, one per column, rather than as 32-byte pieces of 32
+// different lines per store.  A warp's loads read 128 contiguous bytes of a
+// key row each.  Keys in [rows, pitch) get zero codes (loaded as zeros).
 template <int kElem>
 __global__ void __launch_bounds__(256) quant_cols_attn_kernel(
-    const uint32_t* __restrict__ x, int batch, int rows, int log2_cpairs, uint8_t* __restrict__ codes,
+    const uint32_t* __restrict__ x, int rows, int log2_cpairs, uint8_t* __restrict__ codes,
     int pitch, uint8_t* __restrict__ scales) {
+    __shared__ __align__(16) uint8_t tile[128][144];
     const int cpairs = 1 << log2_cpairs;  // D / 2 = 32 or 64
     const int cols = 2 * cpairs;
-    const int rblocks = (rows + 31) / 32;
-    const int n_tiles = (rows + kTile - 1) / kTile;
-    const int total = (batch * rblocks) << log2_cpairs;  // < 2^31, checked by the launcher
-    for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < total; g += gridDim.x * blockDim.x) {
-        const int cp = g & (cpairs - 1);
-        const int t = g >> log2_cpairs;
-        const int b32 = t / rblocks;
-        const int rb = t - b32 * rblocks;
-        const int64_t b = b32;
-        const int r0 = rb * 32;
+    const int n_tiles = gridDim.x;
+    const int rt = blockIdx.x;            // key tile
+    const int64_t b = blockIdx.y;         // head
+    const int cp = threadIdx.x & (cpairs - 1);
+    const int kb = threadIdx.x >> log2_cpairs;  // 32-key block of the tile (blockDim = 4 cpairs)
+    const int r0 = rt * kTile + 32 * kb;
+    if (r0 < rows) {
         const uint32_t* src = x + (b * rows + r0) * cpairs + cp;
         uint32_t w[32];
 #pragma unroll
@@ -443,21 +444,27 @@ __global__ void __launch_bounds__(256) quant_cols_attn_kernel(
             u0[j] = __byte_perm(w[2 * j], w[2 * j + 1], 0x5410);
             u1[j] = __byte_perm(w[2 * j], w[2 * j + 1], 0x7632);
         }
-        // pitch is a multiple of 16 and r0 of 32: each 16-byte half of a
-        // block is entirely inside or entirely outside the padded line; the
-        // padding keys [rows, pitch) receive zero codes (loaded as zeros)
-        const int kb = rb & 3;
-        const int64_t atom = (b * n_tiles + r0 / kTile) * kAtomBytes;
+        const int64_t atom = (b * n_tiles + rt) * kAtomBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t q[8];
             const int X = quantize_block_attn<kElem>(h ? u1 : u0, q);
             const int c = 2 * cp + h;
-            uint4* d4 = reinterpret_cast<uint4*>(codes + (b * cols + c) * static_cast<int64_t>(pitch) + r0);
+            uint4* d4 = reinterpret_cast<uint4*>(&tile[c][32 * kb]);
             d4[0] = make_uint4(q[0], q[1], q[2], q[3]);
-            if (r0 + 16 < pitch) d4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            d4[1] = make_uint4(q[4], q[5], q[6], q[7]);
             scales[atom + atom_offset(c, kb)] = static_cast<uint8_t>(X + 127);
         }
+    }
+    __syncthreads();
+    // the tile's part of each line: up to 128 bytes, a multiple of 16 (pitch
+    // and the tile start are), 8 threads per line
+    const int valid = min(kTile, pitch - rt * kTile) >> 4;
+    for (int i = threadIdx.x; i < cols * 8; i += blockDim.x) {
+        const int c = i >> 3, k = i & 7;
+        if (k < valid)
+            *reinterpret_cast<uint4*>(codes + (b * cols + c) * static_cast<int64_t>(pitch) + rt * kTile + 16 * k) =
+                *reinterpret_cast<const uint4*>(&tile[c][16 * k]);
     }
 }
 
@@ -512,24 +519,20 @@ cudaError_t launch_quant_cols(const uint16_t* x, int64_t batch, int64_t rows, in
     if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
     if (layout == QL_ATTN && (cols == 64 || cols == 128) && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
         (reinterpret_cast<uintptr_t>(codes) & 15) == 0 && code_pitch % 16 == 0 &&
-        code_pitch < (int64_t{1} << 31) && batch * ((rows + 31) / 32) * (cols / 2) < (int64_t{1} << 31)) {
-        // the fused attention's V operand: a thread per column pair and 32 keys
-        int dev = 0, nsm = 148;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        const int64_t total = batch * ((rows + 31) / 32) * (cols / 2);
-        int64_t blocks = (total + 255) / 256;
-        blocks = blocks < static_cast<int64_t>(nsm) * 8 ? blocks : static_cast<int64_t>(nsm) * 8;
+        code_pitch < (int64_t{1} << 31) && batch <= 65535 && rows < (int64_t{1} << 31) - kTile) {
+        // the fused attention's V operand: a CTA per 128-key tile and head, a
+        // thread per column pair and 32-key block
         const uint32_t* x2 = reinterpret_cast<const uint32_t*>(x);
-        const int bt = static_cast<int>(batch), r = static_cast<int>(rows), pt = static_cast<int>(code_pitch);
+        const int r = static_cast<int>(rows), pt = static_cast<int>(code_pitch);
         const int l2 = cols == 128 ? 6 : 5;
-        const unsigned nb = static_cast<unsigned>(blocks);
+        const dim3 grid(static_cast<unsigned>((rows + kTile - 1) / kTile), static_cast<unsigned>(batch));
+        const unsigned threads = 4u << l2;  // 4 blocks of 32 keys x column pairs
         if (elem == ELEM_E4M3)
-            quant_cols_attn_kernel<ELEM_E4M3><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E4M3><<<grid, threads, 0, st>>>(x2, r, l2, codes, pt, scales);
         else if (elem == ELEM_E2M3)
-            quant_cols_attn_kernel<ELEM_E2M3><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E2M3><<<grid, threads, 0, st>>>(x2, r, l2, codes, pt, scales);
         else
-            quant_cols_attn_kernel<ELEM_E2M1><<<nb, 256, 0, st>>>(x2, bt, r, l2, codes, pt, scales);
+            quant_cols_attn_kernel<ELEM_E2M1><<<grid, threads, 0, st>>>(x2, r, l2, codes, pt, scales);
         return cudaGetLastError();
     }
     dim3 grid(static_cast<unsigned>((rows + 31) / 32),
