@@ -642,11 +642,17 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_addr, int D, int wg, 
 // lets the tile run to its end on whatever the buffers hold (nothing is
 // read or written out of bounds); the warp-wide result, false = aborted,
 // ends the loop.
-template <int kP, bool kShortcut = false, bool kSpec = false>
+// Work that must come before a rescale's wait for the previous PV product
+// (none in the one-CTA kernel; see the persistent kernel).
+struct NoHook {
+    __device__ __forceinline__ bool operator()() const { return true; }
+};
+
+template <int kP, bool kShortcut = false, bool kSpec = false, typename Hook = NoHook>
 __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, int g, int it, int wg,
                                              int r, uint32_t lane_addr, uint32_t s_col,
                                              bool row_valid, int64_t grow, bool tail, bool bounded,
-                                             RowState& rs) {
+                                             RowState& rs, const Hook& before_rescale = Hook()) {
     const int D = p.D;
     const int pb = g & (kPBuf - 1);
     bool ok = mbar_wait(&sm.s_full[wg], it & 1, p.timeout_ns, &sm.abort);
@@ -730,7 +736,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
     tc_fence_before();
     warp_arrive(&sm.s_free[wg]);
     if (!extrema_done) {
-        if ((tail)) {
+        if (tail) {
             // keys >= S of a partial last tile are masked before the gate and the conversion
             const int n_valid = p.Sk - t * kTile;
             mask32(s0, n_valid);
@@ -765,7 +771,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         sm.tmax_x[g & 7][r] = tmax;
         warp_arrive(&sm.m_ready[g & 7]);
         if (t > 0) {
-            if ((!have_prev)) {
+            if (!have_prev) {
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
                 prev = sm.tmax_x[ms][r];
             }
@@ -783,8 +789,9 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // the running maximum grows on a large share of tiles: O and l are
         // rescaled after the conversion, so that the wait for the previous
         // PV product overlaps it (P buffer first, as below)
-        if ((!have_p)) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
         if (any_grew) {
+            ok &= before_rescale();
             ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o_all(lane_addr, D, rescale);
         }
@@ -804,7 +811,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // frozen reference: replay the gate over the previous tile's maximum,
         // m_{t-1} = gate(m_{t-2}, tmax_{t-1}); tile 0 initialises it
         if (t > 0) {
-            if ((!have_prev)) {
+            if (!have_prev) {
                 ok &= mbar_wait(&sm.m_ready[ms], m_par, p.timeout_ns, &sm.abort);
                 prev = sm.tmax_x[ms][r];
             }
@@ -824,8 +831,8 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
         // products retire in order, so afterwards the barrier of tile g - 1's
         // buffer is past PV_{g-3} and can only be in the phase of PV_{g-1}
         // itself (PV_{g+1} needs this tile's P).
-        if ((!have_p)) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
-        if ((__any_sync(0xFFFFFFFFu, fire))) {
+        if (!have_p) ok &= mbar_wait(&sm.p_free[pb], pf_par, p.timeout_ns, &sm.abort);
+        if (__any_sync(0xFFFFFFFFu, fire)) {
             // the bitmap was zeroed before the launch: only firings are written
             if (fire && row_valid) {
                 if (p.rollback_bits) p.rollback_bits[grow * p.n_t + t] = 1;
@@ -833,6 +840,7 @@ __device__ __forceinline__ bool softmax_tile(Smem& sm, const Params& p, int t, i
             }
             // recovery: once PV of the previous tile retired, O and l of the
             // firing rows are scaled by exp(m_old - m_new) in TMEM
+            ok &= before_rescale();
             ok &= mbar_wait(&sm.p_free[(g - 1) & 1], ((g - 1) >> 1) & 1, p.timeout_ns, &sm.abort);
             rescale_o(lane_addr, D, rescale);
         }
@@ -1444,21 +1452,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t0 = (wg - g0) & 1;  // this warpgroup's first tile of the item
             // O and l of item j - 1 are released to item j's first PV product
             // as soon as they are read
-            if (owed && !(have && t0 == 0)) {
-                if (ok) ok = wait_warp(&sm.o_full, (j - 1) & 1, p, sm);
-                if (!ok) break;
-                epilogue_row(lane_addr, D, wg, owed_valid, p.o + owed_grow * D, &sm.o_free);
+            auto pay = [&]() -> bool {
+                if (!owed) return true;
+                const bool w = wait_warp(&sm.o_full, (j - 1) & 1, p, sm);
+                if (w) epilogue_row(lane_addr, D, wg, owed_valid, p.o + owed_grow * D, &sm.o_free);
                 owed = false;
+                return w;
+            };
+            // Every warpgroup writes the epilogue it owes after its first tile
+            // of item j; should that tile roll back, before its rescale's wait
+            // for the item's first PV product (which waits for the epilogue).
+            // Six-bit P keeps the epilogue first when its first tile is tile 1
+            // (measured faster so: 1168 against 1015 TFLOP/s with four KV
+            // tiles per item; E4M3 P 1270 against 1090, EFQ 995 against 956).
+            constexpr bool kDeferAll = kP != kPE2M3;
+            const bool defer = have && (kDeferAll ? t0 < p.n_t : t0 == 0);
+            if (owed && !defer) {
+                if (ok) ok = pay();
+                if (!ok) break;
             }
             if (!have) break;
             for (int t = t0; ok && t < p.n_t; t += 2, ++it) {
-                ok = softmax_tile<kP>(sm, p, t, g0 + t, it, wg, r, lane_addr, s_col, row_valid, grow,
-                                      t == t_tail, bounded, rs);
-                if (owed) {  // deferred past tile 0
-                    if (ok) ok = wait_warp(&sm.o_full, (j - 1) & 1, p, sm);
-                    if (ok) epilogue_row(lane_addr, D, wg, owed_valid, p.o + owed_grow * D, &sm.o_free);
-                    owed = false;
-                }
+                if constexpr (kDeferAll)
+                    ok = softmax_tile<kP>(sm, p, t, g0 + t, it, wg, r, lane_addr, s_col, row_valid, grow,
+                                          t == t_tail, bounded, rs, pay);
+                else
+                    ok = softmax_tile<kP>(sm, p, t, g0 + t, it, wg, r, lane_addr, s_col, row_valid, grow,
+                                          t == t_tail, bounded, rs);
+                if (owed) ok = pay() && ok;  // deferred past the first tile
             }
             owed = true;
             owed_valid = row_valid;

@@ -118,3 +118,33 @@ def test_persistent_bounded_wait_reports_timeout_and_context_survives(fsa, n_sm)
     assert fsa.get_device_error() == 0
     ref = oracle.attention(q, k, v, fmt="mxfp4", mode="fused")["out"]
     parity.check_out(f"persistent after timeout mxfp4", to_f64(o).reshape(-1, D), ref)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "mxfp4_efq"])
+def test_persistent_rollback_at_tile_one_with_many_items(fsa, n_sm, fmt):
+    # theta = 0 (every tile whose maximum passes the reference rolls back, so
+    # tile 1 of most items does) with several items per CTA: the rescale of
+    # tile 1 waits for the item's first PV product, which waits for the
+    # previous item's epilogue -- written first by the warpgroup that owes it.
+    # The EFQ producer's growing running maximum takes the same path.
+    B, H, Sq, Sk, D = 1, 8, 10000, 1000, 128
+    assert B * H * ((Sq + 127) // 128) > 3 * n_sm and (Sk + 127) // 128 <= 16
+    q, k, v = _qkv(B, H, Sq, Sk, D, seed=91)
+    n_t = (Sk + 127) // 128
+    bits = torch.full((B * H * Sq, n_t), 7, dtype=torch.uint8, device="cuda")
+    o = fsa.cross_attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt=fmt, threshold=0.0,
+                                rollback_bits=bits if fmt != "mxfp4_efq" else None)
+    st = fsa.get_device_error()
+    assert st == 0, fsa.status_string(st)
+    rows = np.arange(0, B * H * Sq, 7).astype(np.int64)
+    if fmt == "mxfp4_efq":
+        r = oracle.attention(q, k, v, fmt="mxfp4", mode="efq", rows=rows)
+        parity.check_out(f"persistent theta 0 {fmt}", to_f64(o).reshape(-1, D)[rows], r["out"])
+        return
+    r = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=0.0, rows=rows, want_bits=True,
+                         want_margins=True)
+    sel = bits[torch.from_numpy(rows).cuda()].cpu().numpy()
+    skip, _ = parity.check_bits(f"persistent theta 0 {fmt} bits", sel, r["bits"], r["margins"])
+    assert r["bits"][:, 1].sum() > len(rows) // 10      # tile 1 rolls back in many rows
+    parity.check_out(f"persistent theta 0 {fmt}", to_f64(o).reshape(-1, D)[rows], r["out"],
+                     skip_rows=skip)
