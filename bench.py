@@ -17,7 +17,7 @@ the device with the copies overlapping the computation.
   python bench.py --schedule    # 20-step hybrid MXFP6/MXFP4 schedule vs all-BF16 / all-MXFP4
   python bench.py --mma-peaks   # only the tensor-core rate probe
 
-After the timed region the default run also times the task's other
+After the timed region the default run also times the other benchmark
 workloads (`configs`: B=1 H=16 S=8192, the rollback-stress shape, the
 B=1 H=32 sequence sweep with the BF16 kernel) and measures the dense
 block-scaled MMA rates with the library's tensor-core rate probe
@@ -301,7 +301,7 @@ SWEEP_S = (16384, 32768, 65536, 131072)
 
 
 def run_configs(fsa, dev, stream, seed):
-    """The task's other throughput workloads, one warm-up and one timed call
+    """The other benchmark workloads, one warm-up and one timed call
     per format (quantizer and fused kernel timed apart, CUDA events on the
     launching stream): B=1 H=16 S=8192 D=128; the rollback-stress shape
     (B=1 H=8 S=32768 D=128, 1 % of the keys after 16384 scaled by 8; firings
@@ -748,7 +748,7 @@ def main():
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error during e2e")
 
-    # the other workloads of the task's list, then the tensor-core rate probe
+    # the other benchmark workloads, then the tensor-core rate probe
     # (last: it runs the GPU into its power cap)
     configs = None
     if not args.no_configs and not cross:

@@ -446,9 +446,8 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
         convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
         convert32_linear(s3, alpha, beta, linear_kx(sb3), linear_kx2(sb3), mul8, mul16, w3);
-        if ((!__all_sync(0xFFFFFFFFu,
-                                     block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
-                                                     max(max(sb0, sb1), max(sb2, sb3)), alpha, beta)))) {
+        if (!__all_sync(0xFFFFFFFFu, block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                                     max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
             convert32<true>(s0, alpha, beta, general_inv(sb0), mul16, w0);
             convert32<true>(s1, alpha, beta, general_inv(sb1), mul16, w1);
             convert32<true>(s2, alpha, beta, general_inv(sb2), mul16, w2);
@@ -461,9 +460,8 @@ __device__ __forceinline__ uint32_t convert_tile(const uint32_t (&s0)[32], const
     // linearly (the common case for MXFP8), else block by block.  Checked
     // once per row against the largest block threshold (sb grows with the
     // block maximum), which implies every block's own condition.
-    if (kE4M3 && (__all_sync(0xFFFFFFFFu,
-                            block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
-                                            max(max(sb0, sb1), max(sb2, sb3)), alpha, beta)))) {
+    if (kE4M3 && __all_sync(0xFFFFFFFFu, block_is_linear(fminf(fminf(bmin[0], bmin[1]), fminf(bmin[2], bmin[3])),
+                                                         max(max(sb0, sb1), max(sb2, sb3)), alpha, beta))) {
         convert32_linear(s0, alpha, beta, linear_kx(sb0), linear_kx2(sb0), mul8, mul16, w0);
         convert32_linear(s1, alpha, beta, linear_kx(sb1), linear_kx2(sb1), mul8, mul16, w1);
         convert32_linear(s2, alpha, beta, linear_kx(sb2), linear_kx2(sb2), mul8, mul16, w2);
