@@ -300,6 +300,44 @@ CONFIG_FORMATS = ("mxfp8", "mxfp6", "mxfp4", "mxfp4_efq")
 SWEEP_S = (16384, 32768, 65536, 131072)
 
 
+def host_copy_rates(h_in, h_out, dev, reps=3):
+    """Pinned host <-> device copy rates (GB/s) of this box: h_in -> device
+    alone, device -> h_out alone, and both at once on two streams; CUDA
+    events on the copy streams, the best of `reps`."""
+    d_in, d_out = torch.empty_like(h_in, device=dev), torch.empty_like(h_out, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    b_in, b_out = h_in.numel() * h_in.element_size(), h_out.numel() * h_out.element_size()
+    best = {"h2d": 0.0, "d2h": 0.0, "h2d_while_d2h": 0.0, "d2h_while_h2d": 0.0}
+    torch.cuda.synchronize(dev)
+    def copy_in():
+        with torch.cuda.stream(s_in):
+            ev[0].record(s_in)
+            d_in.copy_(h_in, non_blocking=True)
+            ev[1].record(s_in)
+
+    def copy_out():
+        with torch.cuda.stream(s_out):
+            ev[2].record(s_out)
+            h_out.copy_(d_out, non_blocking=True)
+            ev[3].record(s_out)
+
+    for _ in range(reps):
+        copy_in()
+        torch.cuda.synchronize(dev)
+        best["h2d"] = max(best["h2d"], b_in / (ev[0].elapsed_time(ev[1]) * 1e6))
+        copy_out()
+        torch.cuda.synchronize(dev)
+        best["d2h"] = max(best["d2h"], b_out / (ev[2].elapsed_time(ev[3]) * 1e6))
+        copy_in()
+        copy_out()
+        torch.cuda.synchronize(dev)
+        best["h2d_while_d2h"] = max(best["h2d_while_d2h"], b_in / (ev[0].elapsed_time(ev[1]) * 1e6))
+        best["d2h_while_h2d"] = max(best["d2h_while_h2d"], b_out / (ev[2].elapsed_time(ev[3]) * 1e6))
+    del d_in, d_out
+    return best
+
+
 def run_configs(fsa, dev, stream, seed):
     """The other benchmark workloads, one warm-up and one timed call
     per format (quantizer and fused kernel timed apart, CUDA events on the
@@ -747,6 +785,12 @@ def main():
                        "with copies overlapping compute)"}
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error during e2e")
+        # the box's pinned host copy rates, to read the end-to-end figure by:
+        # one direction alone, then both at once (the pipeline's case)
+        e2e["host_copy_gbs"] = host_copy_rates(hq, ho, dev)
+        e2e["copy_ms_per_step_at_these_rates"] = 1e3 * max(
+            e2e["h2d_bytes_per_step"] / (1e9 * e2e["host_copy_gbs"]["h2d_while_d2h"]),
+            e2e["d2h_bytes_per_step"] / (1e9 * e2e["host_copy_gbs"]["d2h_while_h2d"]))
 
     # the other benchmark workloads, then the tensor-core rate probe
     # (last: it runs the GPU into its power cap)
