@@ -767,14 +767,19 @@ def main():
         torch.cuda.synchronize(dev)
         if pg:
             pg.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        # an event after every call, so that the line also shows how evenly
+        # the calls ran (each call's span on the caller's stream)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(FORMATS) * args.steps + 1)]
+        evs[0].record(stream)
+        n_ev = 1
         for fmt in FORMATS:            # format-major, as the device-timed region
             for _ in range(args.steps):
                 e2e_call(fmt)
-        e1.record(stream)
+                evs[n_ev].record(stream)
+                n_ev += 1
         torch.cuda.synchronize(dev)
-        te = e0.elapsed_time(e1) / 1e3
+        te = evs[0].elapsed_time(evs[-1]) / 1e3
+        spans = [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
         if pg:
             te = max_over_ranks(te, pg, dev)
         nbytes = tq.numel() * 2
@@ -782,7 +787,9 @@ def main():
                "h2d_bytes_per_step": len(FORMATS) * (nbytes + 2 * tk.numel() * 2),
                "d2h_bytes_per_step": len(FORMATS) * nbytes,
                "call": "fsa_attention_fwd_host per format (pinned host buffers; chunks of heads "
-                       "with copies overlapping compute)"}
+                       "with copies overlapping compute)",
+               "call_ms": {fmt: [round(x, 2) for x in spans[i * args.steps:(i + 1) * args.steps]]
+                           for i, fmt in enumerate(FORMATS)}}
         if fsa.get_device_error() != 0:
             raise RuntimeError("device error during e2e")
         # the box's pinned host copy rates, to read the end-to-end figure by:

@@ -64,6 +64,10 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kHelperRegs <= kThreads * kLaunchRe
 // (measured on GB300 with 75600 query rows x 40 heads: faster up to 2048
 // keys, even at 4096, slower at 8192), whatever the number of items.
 constexpr int kPersistentMaxTiles = 16;
+// The EFQ producer's persistent kernel also wins at 64 and 128 KV tiles per
+// item (B=1 H=16 S=8192: 1248 -> 1335 TFLOP/s; H=32 S=16384: 1460 -> 1506)
+// and loses at 591 (1758 -> 1687).
+constexpr int kPersistentMaxTilesEfq = 128;
 // The persistent kernel's helper warps keep the rings' state across work
 // items and give back only to 40: 2 * 128 * 232 + 128 * 40 = 64512.
 constexpr int kHelperRegsPersistent = 40;
@@ -597,9 +601,12 @@ __device__ __forceinline__ void rescale_o_all(uint32_t lane_addr, int D, float r
 // FP32 place of O / l, before the bf16 rounding): on items of a few KV tiles
 // an IEEE division per element cost a third of the item's instructions
 // (measured 785 -> 1086 TFLOP/s with four tiles per item).  The one-CTA
-// kernel divides (once per CTA of many tiles it costs nothing, and its main
-// loop measured faster so compiled); which kernel a call takes depends only
-// on the key length, so calls with the same keys compute the same bytes.
+// kernel of E4M3 P ends the same way (its epilogue took 2.8 us of a CTA's
+// 42 us with 64 KV tiles when it divided: +4 % there, +1.5 % with 128
+// tiles); the six-bit and EFQ one-CTA kernels divide, their main loops
+// measured faster so compiled.  Which kernel a call takes depends only on
+// the key length and format, so calls with the same keys compute the same
+// bytes.
 __device__ __forceinline__ void epilogue_chunk(const uint32_t (&rr)[32], float l, uint4* dst) {
     const float inv = __frcp_rn(l);
     uint32_t packed[16];
@@ -1103,28 +1110,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             // epilogue: warpgroup wg writes columns [wg * D/2, (wg+1) * D/2)
-            tc_fence_after();
-            uint32_t lv;
-            tmem_ld1(lane_addr + kColO + D, lv);
-            tmem_ld_wait();
-            const float l = __uint_as_float(lv);
-            for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
-                uint32_t rr[32];
-                tmem_ld32(lane_addr + kColO + 32 * c, rr);
+            if constexpr (kP == kPE4M3) {
+                epilogue_row(lane_addr, D, wg, row_valid, p.o + grow * D, nullptr);
+            } else {
+                tc_fence_after();
+                uint32_t lv;
+                tmem_ld1(lane_addr + kColO + D, lv);
                 tmem_ld_wait();
-                tmem_reg_dep(rr);
-                if (row_valid) {
-                    uint32_t packed[16];
+                const float l = __uint_as_float(lv);
+                for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(lane_addr + kColO + 32 * c, rr);
+                    tmem_ld_wait();
+                    tmem_reg_dep(rr);
+                    if (row_valid) {
+                        uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * j]), l),
-                                                                  __fdiv_rn(__uint_as_float(rr[2 * j + 1]), l));
-                        packed[j] = *reinterpret_cast<uint32_t*>(&h2);
+                        for (int j = 0; j < 16; ++j) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(__fdiv_rn(__uint_as_float(rr[2 * j]), l),
+                                                                      __fdiv_rn(__uint_as_float(rr[2 * j + 1]), l));
+                            packed[j] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + grow * D + 32 * c);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
                 }
             }
             if (p.rollback_count) {
@@ -1556,12 +1567,13 @@ cudaError_t launch_fsa_attention(const AttnLaunch& a, cudaStream_t st) {
     // short key sequences: the per-CTA set-up and pipeline fill would
     // dominate a CTA that runs only a few KV tiles, so persistent CTAs (one
     // per SM, at most one per work item) walk the work items instead.  The
-    // choice depends on the key length alone, not on the number of items,
-    // so every call with the same keys -- a whole tensor or the chunks of
-    // heads of the host-buffer entry points -- takes the same kernel
-    // the shortcut gate exists as a variant of the one-CTA-per-item kernel
+    // choice depends on the key length and the format alone, not on the
+    // number of items, so every call with the same keys -- a whole tensor or
+    // the chunks of heads of the host-buffer entry points -- takes the same
+    // kernel.  The shortcut gate exists as a variant of the
+    // one-CTA-per-item kernel.
     const bool shortcut = a.gate_mode == 1 && a.fmt != 3;
-    const bool persistent = !shortcut && p.n_t <= kPersistentMaxTiles;
+    const bool persistent = !shortcut && p.n_t <= (a.fmt == 3 ? kPersistentMaxTilesEfq : kPersistentMaxTiles);
     // P in E4M3 for MXFP8, six-bit E2M3 for MXFP6 and MXFP4, E2M1 codes of
     // the EFQ producer for MXFP4-EFQ
     using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const Params);

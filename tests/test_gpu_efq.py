@@ -71,3 +71,20 @@ def test_efq_full_size_sampled(fsa):
     got = to_f64(o).reshape(-1, D)[rows]
     ref = oracle.attention(q, k, v, fmt="mxfp4", mode="efq", rows=rows)["out"]
     parity.check_out(f"efq h16-s8192", got, ref)
+
+
+@pytest.mark.parametrize("S", [16384, 16385])
+def test_efq_at_the_persistent_boundary(fsa, S):
+    # 128 KV tiles per item run the EFQ producer's persistent kernel, 129 (a
+    # ragged last tile of one key) the one-CTA-per-item kernel; the growing
+    # maximum of the second half rescales O and l in both
+    B, H, D = 1, 2, 128
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=74, stress_from=S // 2)
+    o = fsa.attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt="mxfp4_efq")
+    assert fsa.get_device_error() == 0
+    rng = np.random.default_rng(74)
+    rows = np.unique(np.concatenate([np.arange(128), (B * H - 1) * S + np.arange(S - 128, S),
+                                     rng.integers(0, B * H * S, 128)])).astype(np.int64)
+    got = to_f64(o).reshape(-1, D)[rows]
+    ref = oracle.attention(q, k, v, fmt="mxfp4", mode="efq", rows=rows)["out"]
+    parity.check_out(f"efq boundary S={S}", got, ref)

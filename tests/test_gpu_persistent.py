@@ -1,4 +1,5 @@
-"""GPU parity of the persistent kernel (work items of at most 16 KV tiles:
+"""GPU parity of the persistent kernel (work items of at most 16 KV tiles,
+128 for the EFQ producer, whose larger items tests/test_gpu_efq.py covers:
 one CTA per SM, at most one per item, walks the items with double-buffered Q
 and barrier phases carried across items; the cases here have more items than
 SMs, so every CTA walks several) against the CPU oracle.  Same bar as the
