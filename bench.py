@@ -257,15 +257,25 @@ def to_dev(bits, device):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
 
 
+def sample_rows(w, n_rows):
+    """Rows of an oracle sample: n_rows rows of the video-DiT key length's
+    work, i.e. n_rows * 75600 / Sk rows (at most every row), evenly spaced
+    over all heads."""
+    total = w["B"] * w["H"] * w["S"]
+    n = min(total, max(1, round(n_rows * WORKLOADS["video-dit"]["S"] / keys(w))))
+    return np.unique(np.linspace(0, total - 1, n).astype(np.int64))
+
+
 def oracle_sample(q, k, v, w, fmt, n_rows, threads):
-    """Time the oracle on n_rows query rows of the first head."""
+    """Time the oracle on the rows of sample_rows(w, n_rows); returns the
+    sample's FLOPs, seconds and row count."""
     import oracle
-    rows = np.linspace(0, w["S"] - 1, n_rows).astype(np.int64)
+    rows = sample_rows(w, n_rows)
     t0 = time.perf_counter()
     oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=THRESHOLD, rows=rows,
                      threads=threads)
     dt = time.perf_counter() - t0
-    return n_rows * 4.0 * keys(w) * w["D"], dt
+    return len(rows) * 4.0 * keys(w) * w["D"], dt, len(rows)
 
 
 def max_over_ranks(x, dist=None, device="cpu"):
@@ -457,15 +467,15 @@ def run_reference(args, w, rank, world):
     for i in range(args.warmup + args.steps):
         f_step, t_step = 0.0, 0.0
         for fmt in FORMATS:
-            f, t = oracle_sample(q, k, v, w, fmt, n_rows, threads)
+            f, t, n_used = oracle_sample(q, k, v, w, fmt, n_rows, threads)
             f_step += f
             t_step += t
         if i >= args.warmup:
             total_f += f_step
             total_t += t_step
     val = total_f / total_t / 1e12
-    sample = (f"{n_rows} query rows of head 0 per format per step (all keys), "
-              f"3 formats; rate extrapolates exactly since rows are independent")
+    sample = (f"{n_used} query rows evenly spaced over all heads per format per step (all "
+              f"{keys(w)} keys), 3 formats; rate extrapolates exactly since rows are independent")
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
@@ -829,10 +839,10 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         threads, affinity = cpu_affinity()
-        f, t = oracle_sample(q, k, v, w, "mxfp8", args.cpu_rows, threads)
+        f, t, n_used = oracle_sample(q, k, v, w, "mxfp8", args.cpu_rows, threads)
         cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": threads, "affinity": affinity,
                "kind": "oracle",
-               "sample": f"{args.cpu_rows} query rows of head 0 (all {Sk} keys), MXFP8, "
+               "sample": f"{n_used} query rows evenly spaced over all heads (all {Sk} keys), MXFP8, "
                          f"{t:.1f} s; rows are independent so the rate extrapolates exactly"}
 
     a8 = per_format["mxfp8"]
