@@ -12,8 +12,10 @@ The bar (the same in every parity test):
     moves each of its weights by up to half a step of the coarser grid (6 %
     for E4M3), and a row whose weight sits mostly in that block moves about
     as much.  Measured on GB300 over all the parity tests: the largest row
-    error 4.9e-2 (rows dominated by one key), rows above TOL at most 0.4 %
-    of a large sample; a corrupted value gives errors of order one.  Rows
+    error 4.9e-2 (rows dominated by one key); rows above TOL 0.26-1.05 % of
+    a sample of 1526 rows (MXFP6, ten seeds of B=1 H=16 S=8192, mean 0.67 %;
+    MXFP8 at most 0.4 %), so the count bound sits at twice the largest; a
+    corrupted value gives errors of order one.  Rows
     whose gate decision legitimately differs -- a near-tie -- are left out
     of the per-row bounds, see below;
   * rollback decisions: identical per (row, tile) except near-ties, tiles
@@ -36,7 +38,7 @@ import numpy as np
 
 TOL = 5e-3
 ROW_TOL = 0.1
-MAX_ROWS_ABOVE_TOL = 0.01
+MAX_ROWS_ABOVE_TOL = 0.02
 NEAR_TIE = 1e-4
 MAX_NEAR_TIE_FRAC = 1e-3
 

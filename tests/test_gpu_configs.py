@@ -3,11 +3,10 @@ measured on, through the C ABI, at full size with sampled rows:
 
   * the video-DiT self-attention shape (B=1 H=40 S=75600 D=128: 21 x 45 x
     80 latent tokens of the pages' video model, "Fused-Softmax shifts ...",
-    paragraph 9), every format, including EFQ-Softmax -- the first and last
-    query tile and random rows of the first and the last head (the last KV
-    tile holds 80 keys);
+    paragraph 9), every format, including EFQ-Softmax (the last KV tile
+    holds 80 keys);
   * B=1 H=16 S=8192 D=128, ten seeds (the pages' synthetic error study,
-    paragraph 7), every format, 128 rows per seed; the same sample also
+    paragraph 7), every format; the same sample also
     reproduces the pages' error split from the GPU's output: totals within
     1 percentage point of 5.69 / 6.46 / 20.53 % against FP64 softmax
     attention, and at most 0.3 pp (+0.1 pp sampling tolerance) above
@@ -15,7 +14,10 @@ measured on, through the C ABI, at full size with sampled rows:
   * the rollback-stress shape (B=1 H=8 S=32768 D=128, 1 % of the keys after
     16384 scaled by 8) in every method format, with the rollback decision
     of every sampled (row, tile).
-The bar is the one of tests/parity.py."""
+Each samples every row of the first and last query tile of the first and the
+last head (and of the middle head for the stress shape, where the stressed
+keys start) plus 1024 rows drawn over the whole tensor.  The bar is the one
+of tests/parity.py."""
 import math
 import os
 
@@ -40,14 +42,15 @@ def fsa():
     return m
 
 
-def _rows_of_heads(S, heads, n_random, seed):
-    """First and last query tile plus n_random random rows of each head."""
-    rng = np.random.default_rng(seed + 1000)
+def _sample_rows(BH, S, seed, heads=()):
+    """The parity sample of a full-size workload: every row of the first and
+    the last query tile of head 0, of the last head and of `heads`, plus
+    1024 rows drawn over the whole tensor from seed + 1000."""
     last0 = ((S - 1) // 128) * 128
     rows = []
-    for h in heads:
-        rows += [h * S + np.arange(0, min(128, S)), h * S + np.arange(last0, S),
-                 h * S + rng.integers(0, S, n_random)]
+    for h in sorted({0, BH - 1, *heads}):
+        rows += [h * S + np.arange(0, min(128, S)), h * S + np.arange(last0, S)]
+    rows.append(np.random.default_rng(seed + 1000).integers(0, BH * S, 1024))
     return np.unique(np.concatenate(rows)).astype(np.int64)
 
 
@@ -62,7 +65,7 @@ def video_dit(fsa):
     B, H, S, D = 1, 40, 75600, 128
     q, k, v = fsa_inputs.qkv(B, H, S, D, seed=0)
     dev = tuple(to_dev(x) for x in (q, k, v))
-    rows = _rows_of_heads(S, (0, B * H - 1), 64, seed=0)
+    rows = _sample_rows(B * H, S, seed=0)
     yield q, k, v, dev, rows
     del dev
     torch.cuda.empty_cache()
@@ -114,9 +117,7 @@ def test_h16_s8192_ten_seeds_and_the_pages_error_split(fsa):
     for seed in range(10):
         q, k, v = fsa_inputs.qkv(B, H, S, D, seed=seed)
         tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
-        rows = _rows_of_heads(S, (0, B * H - 1), 0, seed)[::4]          # 128 fixed rows
-        rng = np.random.default_rng(seed + 2000)
-        rows = np.unique(np.concatenate([rows, rng.integers(0, B * H * S, 64)])).astype(np.int64)
+        rows = _sample_rows(B * H, S, seed)
         exact = oracle.attention(q, k, v, fmt=None, mode="exact", rows=rows)["out"]
         for fmt in tot:
             cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
@@ -152,7 +153,7 @@ def test_rollback_stress_full_size_every_format(fsa, fmt):
                           rollback_bits=rb, rollback_count=cnt)
     st = fsa.get_device_error()
     assert st == 0, fsa.status_string(st)
-    rows = _rows_of_heads(S, (0, B * H // 2, B * H - 1), 48, seed=1)
+    rows = _sample_rows(B * H, S, seed=0, heads=(B * H // 2,))
     r = oracle.attention(q, k, v, fmt=fmt, mode="fused", rows=rows, want_bits=True,
                          want_margins=True)
     sel = rb[torch.from_numpy(rows).cuda()].cpu().numpy()
