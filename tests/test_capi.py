@@ -103,6 +103,14 @@ def test_quantize_argument_validation(lib):
     assert lib.fsa_quantize_mx(P(16), 0, 4, 4, 1, 0, P(16), P(16), None) == 0
 
 
+def test_mma_rate_probe_argument_validation(lib):
+    # every check is on the host, before the device is touched
+    fl = ctypes.c_double(0.0)
+    for kind, ctas, iters in [(-1, 1, 1), (5, 1, 1), (0, 0, 1), (0, 65536, 1), (0, 1, 0),
+                              (0, 1, (1 << 24) + 1)]:
+        assert lib.fsa_mma_rate_probe(kind, ctas, iters, ctypes.byref(fl), None) == 1
+
+
 def test_host_attention_argument_validation(lib):
     # host-buffer entry points: shape, format and threshold checks happen on
     # the host before any device call (host pointers need no alignment)
