@@ -93,8 +93,8 @@ def make_inputs(w, seed):
 
 
 def peaks(mma=None):
-    """Roofline denominators (TFLOP/s, GB/s).  bf16 and HBM: the driver's
-    measurement (MEASURED_PEAKS.json: cuBLAS GEMM, copy).  Block-scaled MMA
+    """Roofline denominators (TFLOP/s, GB/s).  bf16 and HBM: the measured
+    figures of this machine pool (MEASURED_PEAKS.json: cuBLAS GEMM, copy).  Block-scaled MMA
     rates: the tensor-core rate probe of this run (measure_mma_peaks) when
     given -- R8 (E4M3), R6 (E2M3), R4 (packed E2M1, kind::mxf4) and the
     attention kernel's own product mix -- else the bf16 rate times the
