@@ -562,7 +562,10 @@ def main():
     ap.add_argument("--mma-peaks", action="store_true",
                     help="only measure the tensor-core rates and print them")
     ap.add_argument("--cpu-rows", type=int, default=12288)
-    ap.add_argument("--ref-rows", type=int, default=96)
+    # rows of the reference arm's sample per format and step: every oracle
+    # call also quantizes the whole Q, K and V once, so a few rows would time
+    # mostly that (96 rows: 0.004 TFLOP/s against 0.043 for 12288)
+    ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--schedule", action="store_true",
                     help="time the 20-step hybrid precision schedule against all-BF16 and all-MXFP4")
     args = ap.parse_args()
