@@ -40,3 +40,24 @@ def test_reference_arm_other_ranks_exit_without_output():
                        capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_oracle_sample_rows():
+    # the oracle legs' row samples: the video-DiT key length's work in rows,
+    # never more rows than exist, within as few heads from the first on as
+    # hold them (a head's rows share its keys)
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for name, w in bench.WORKLOADS.items():
+        S, total, Sk = w["S"], w["B"] * w["H"] * w["S"], bench.keys(w)
+        for n_rows in (1, 96, 1024, 12288):
+            rows = bench.sample_rows(w, n_rows)
+            want = min(total, max(1, round(n_rows * 75600 / Sk)))
+            assert len(rows) == want, (name, n_rows, len(rows), want)
+            assert rows[0] == 0 and rows[-1] < total
+            assert all(rows[1:] > rows[:-1])
+            heads_needed = -(-want // S)
+            assert rows[-1] < heads_needed * S, (name, n_rows)
+    assert bench.sample_rows(bench.WORKLOADS["video-dit"], 12288)[-1] < 75600
