@@ -31,7 +31,10 @@ def _qkv(B, H, Sq, Sk, D, seed, stress_from=None):
 
 
 CROSS = [(1, 2, 37, 300, 64), (1, 2, 300, 37, 128), (2, 1, 129, 1000, 128), (1, 2, 1000, 129, 64),
-         (1, 1, 1, 513, 128), (1, 3, 640, 128, 64), (1, 1, 256, 1, 128)]
+         (1, 1, 1, 513, 128), (1, 3, 640, 128, 64), (1, 1, 256, 1, 128),
+         # one query row against many KV tiles (one CTA walks 157 of them), and
+         # a few rows against one key more than 32 tiles (a one-key tail tile)
+         (1, 1, 1, 20000, 128), (2, 1, 3, 4097, 64)]
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp6", "mxfp4"])
