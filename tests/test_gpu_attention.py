@@ -154,3 +154,27 @@ def test_gate_at_theta_zero(fsa, fmt):
     assert r["rollback_count"] > 100
     assert cnt == int(rb.sum().item())
     parity.check_out(f"theta 0 {fmt}", to_f64(o).reshape(-1, D), r["out"], skip_rows=skip)
+
+
+@pytest.mark.parametrize("fmt,gate", [("mxfp8", "fp32"), ("mxfp6", "fp32"), ("mxfp4_efq", "fp32"),
+                                      ("mxfp8", "shortcut")])
+def test_maximum_head_count(fsa, fmt, gate):
+    # B * H = 65535, the largest the entry points accept (the launch grids'
+    # y limit): the quantizers' per-head grids, the persistent kernel with
+    # 65535 work items and, through the shortcut gate's one-CTA-per-item
+    # kernel, a grid of 65535 heads; three keys and ragged query tiles
+    B, H, S, D = 3, 21845, 3, 64
+    q, k, v = fsa_inputs.qkv(B, H, S, D, seed=91)
+    o = fsa.attention_fwd(to_dev(q), to_dev(k), to_dev(v), fmt=fmt, threshold=8.0, gate=gate)
+    st = fsa.get_device_error()
+    assert st == 0, fsa.status_string(st)
+    rng = np.random.default_rng(91)
+    BHS = B * H * S
+    rows = np.unique(np.concatenate([np.arange(6), BHS - 6 + np.arange(6),
+                                     rng.integers(0, BHS, 512)])).astype(np.int64)
+    got = to_f64(o).reshape(-1, D)[rows]
+    if fmt == "mxfp4_efq":
+        ref = oracle.attention(q, k, v, fmt="mxfp4", mode="efq", rows=rows)["out"]
+    else:
+        ref = oracle.attention(q, k, v, fmt=fmt, mode="fused", threshold=8.0, gate=gate, rows=rows)["out"]
+    parity.check_out(f"max heads {fmt} {gate}", got, ref)
